@@ -1,0 +1,217 @@
+"""Python binding of the ``libmxq`` C ABI (include/mxq.h).
+
+Argument marshalling only: every step of the quantizers and the GEMM runs in
+the library's sm_103a kernels.  PyTorch supplies device memory and the
+current stream.  There is no fallback: if ``libmxq.so`` is missing or fails
+to load, every call raises.
+
+Entry points (same names as the C ABI):
+  mx_quantize, mx_dequantize, fp8_quantize_pertensor, mx_gemm, sf_to_mma,
+  last_device_status; plus ``quantize`` / ``quantize_dual`` with the
+  argument order of AstrAI's fp8 adapter (astrai/extension/ops/fp8.py).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmxq.so")
+
+E4M3, E5M2, E2M1 = 0, 1, 2
+ROW, COL, DUAL = 1, 2, 3
+FLOOR_OCP, CEIL = 0, 1
+RNE, SR = 0, 1
+SF_CANONICAL, SF_MMA = 0, 1
+
+_FMT = {"e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1, E4M3: E4M3, E5M2: E5M2, E2M1: E2M1}
+_ORIENT = {"row": ROW, "col": COL, "dual": DUAL, ROW: ROW, COL: COL, DUAL: DUAL}
+_SCALE = {"floor": FLOOR_OCP, "floor_ocp": FLOOR_OCP, "ceil": CEIL, FLOOR_OCP: FLOOR_OCP, CEIL: CEIL}
+_ROUND = {"rne": RNE, "sr": SR, "stochastic": SR, RNE: RNE, SR: SR}
+_SF = {"canonical": SF_CANONICAL, "mma": SF_MMA, SF_CANONICAL: SF_CANONICAL, SF_MMA: SF_MMA}
+
+_lib = None
+
+
+class MXQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = _lib.mxq_strerror(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load libmxq.so (built in-tree by ``build()``).  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU or PyTorch fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+    L.mxq_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, i32, i32, u64, u64, i32, vp, vp, vp, vp, vp]
+    L.mxq_dequantize.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
+    L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
+    L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
+    L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
+    L.mxq_last_device_status.argtypes = [vp]
+    L.mxq_strerror.argtypes = [i32]
+    L.mxq_strerror.restype = ctypes.c_char_p
+    L.mxq_version.argtypes = []
+    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_sf_to_mma",
+                 "mxq_last_device_status", "mxq_version"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MXQError(rc, what)
+
+
+def _cuda_2d(x: torch.Tensor, name: str):
+    if not x.is_cuda or x.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D CUDA tensor")
+
+
+# --------------------------------------------------------------------------- MX quantize
+def mx_quantize(x: torch.Tensor, fmt="e4m3", orientation="row", scale_mode="floor", rounding="rne",
+                hadamard32: bool = False, sr_key: int = 0, hadamard_seed: int = 7, sf_layout="canonical"):
+    """MX-quantize bf16 ``x`` [rows][cols] (row stride may exceed cols).
+
+    Returns (q_row, s_row, q_col, s_col); entries for an orientation not
+    requested are None.  q_col / s_col are the transposed column copy."""
+    _cuda_2d(x, "x")
+    if x.dtype != torch.bfloat16 or x.stride(1) != 1:
+        raise ValueError("x must be bf16 with a contiguous last dimension")
+    f, o = _FMT[fmt], _ORIENT[orientation]
+    rows, cols = x.shape
+    dev = x.device
+    qb = 2 if f == E2M1 else 1
+    q_row = s_row = q_col = s_col = None
+    if o & ROW:
+        q_row = torch.empty(rows, cols // qb, dtype=torch.uint8, device=dev)
+        s_row = torch.empty(rows, cols // 32, dtype=torch.uint8, device=dev)
+    if o & COL:
+        q_col = torch.empty(cols, rows // qb, dtype=torch.uint8, device=dev)
+        s_col = torch.empty(cols, rows // 32, dtype=torch.uint8, device=dev)
+    rc = load().mxq_quantize(_ptr(x), rows, cols, x.stride(0), f, o, _SCALE[scale_mode], _ROUND[rounding],
+                             int(bool(hadamard32)), sr_key & (2**64 - 1), hadamard_seed & (2**64 - 1),
+                             _SF[sf_layout], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(dev))
+    _check(rc, "mxq_quantize")
+    return q_row, s_row, q_col, s_col
+
+
+def mx_dequantize(q: torch.Tensor, s: torch.Tensor, fmt="e4m3", out_dtype=torch.float32) -> torch.Tensor:
+    """Dequantize codes ``q`` with canonical scales ``s`` -> float32 or bf16."""
+    _cuda_2d(q, "q")
+    f = _FMT[fmt]
+    rows = q.shape[0]
+    cols = q.shape[1] * (2 if f == E2M1 else 1)
+    out = torch.empty(rows, cols, dtype=out_dtype, device=q.device)
+    rc = load().mxq_dequantize(_ptr(q), _ptr(s), rows, cols, f, int(out_dtype == torch.float32), _ptr(out),
+                               _stream(q.device))
+    _check(rc, "mxq_dequantize")
+    return out
+
+
+# --------------------------------------------------------------------------- per-tensor FP8
+def fp8_quantize_pertensor(x: torch.Tensor, scale: torch.Tensor, fmt="e4m3", orientation="row",
+                           ring_state: Optional[torch.Tensor] = None, hist_idx: int = 0,
+                           fp8_max: float = 448.0, pow2_margin: float = 1.0):
+    """Per-tensor FP8 quantize with fused amax (and the delayed-scaling fold
+    when ``ring_state`` is given).  Returns (x8, x8T, amax); ``amax`` is a
+    fresh 1-element float32 tensor, or, with a ring, a view of the ring's
+    amax slot (which the fold leaves at zero)."""
+    _cuda_2d(x, "x")
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be contiguous bf16")
+    f, o = _FMT[fmt], _ORIENT[orientation]
+    if f not in (E4M3, E5M2):
+        raise ValueError(f"unsupported fp8 format {fmt!r} (expected 'e4m3' or 'e5m2')")
+    rows, cols = x.shape
+    dev = x.device
+    x8 = torch.empty(rows, cols, dtype=torch.uint8, device=dev) if o & ROW else None
+    x8T = torch.empty(cols, rows, dtype=torch.uint8, device=dev) if o & COL else None
+    n = 0
+    if ring_state is not None:
+        n = ring_state.numel() - 4
+        amax = ring_state[n + 2:n + 3]
+        amax_out = None
+    else:
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        amax_out = amax
+    rc = load().fp8_quantize_pertensor(_ptr(x), rows, cols, _ptr(scale), f, o, _ptr(ring_state), n, hist_idx,
+                                       float(fp8_max), float(pow2_margin), _ptr(x8), _ptr(x8T), _ptr(amax_out),
+                                       _stream(dev))
+    _check(rc, "fp8_quantize_pertensor")
+    return x8, x8T, amax
+
+
+def quantize(x, scale, fmt="e4m3", transposed=False, ring_state=None, hist_idx=0, fp8_max=448.0,
+             pow2_margin=1.0):
+    """(x8 | x8T, amax), argument order of AstrAI's ``quantize``."""
+    x8, x8T, amax = fp8_quantize_pertensor(x, scale, fmt, "col" if transposed else "row", ring_state, hist_idx,
+                                           fp8_max, pow2_margin)
+    return (x8T if transposed else x8), amax
+
+
+def quantize_dual(x, scale, fmt="e4m3", ring_state=None, hist_idx=0, fp8_max=448.0, pow2_margin=1.0):
+    """(x8, x8T, amax) from one read, argument order of AstrAI's ``quantize_dual``."""
+    return fp8_quantize_pertensor(x, scale, fmt, "dual", ring_state, hist_idx, fp8_max, pow2_margin)
+
+
+def ring_state_new(hist_len: int = 16, device="cuda") -> torch.Tensor:
+    """Fresh ring [hist | scale | legacy | amax | done]: hist 0, scale 1, legacy 1, amax 0, done 0."""
+    r = torch.zeros(hist_len + 4, dtype=torch.float32, device=device)
+    r[hist_len] = 1.0
+    r[hist_len + 1] = 1.0
+    return r
+
+
+# --------------------------------------------------------------------------- GEMM
+def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.Tensor, fmt="e4m3",
+            out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None) -> torch.Tensor:
+    """C = A * B^T from MX operands (A [M][K], B [N][K] codes, scales in the
+    MMA layout).  Returns bf16 (or float32) [M][N]."""
+    f = _FMT[fmt]
+    M = a_q.shape[0]
+    N = b_q.shape[0]
+    if K is None:
+        K = a_q.shape[1] * (2 if f == E2M1 else 1)
+    c = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    rc = load().mxq_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout], _ptr(c),
+                         int(out_dtype == torch.float32), _stream(a_q.device))
+    _check(rc, "mxq_gemm")
+    return c
+
+
+def sf_to_mma(s: torch.Tensor) -> torch.Tensor:
+    """Canonical scales [rows][kb] -> the GEMM's 512-byte-chunk layout (flat)."""
+    out = torch.empty(s.numel(), dtype=torch.uint8, device=s.device)
+    rc = load().mxq_sf_to_mma(_ptr(s), s.shape[0], s.shape[1], _ptr(out), _stream(s.device))
+    _check(rc, "mxq_sf_to_mma")
+    return out
+
+
+def last_device_status(device=None) -> int:
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return load().mxq_last_device_status(_stream(dev))

@@ -1,0 +1,739 @@
+// Quantizers of bf16 tensors on sm_103a: MX block quantization (row / column
+// / dual orientation, E4M3 / E5M2 / E2M1, floor or ceil scales, RNE or
+// Philox stochastic rounding, optional fixed-sign Hadamard-32) and the
+// per-tensor FP8 quantize with fused amax and the delayed-scaling fold.
+//
+// Sources: "UE8M0 FP8 / MXFP8 explainer", sections 1 and 4, gap sections 1-2
+// (MX blocks of 32 sharing a UE8M0 scale taken from the block amax,
+// saturating element quantization, floor versus ceil scale rounding, row and
+// transposed column copies); AstrAI astrai/extension/ops/fp8.py (quantize /
+// quantize_dual docstrings and commit message: per-tensor multiplier, fused
+// amax, one read for x8 and x8T, last-block fold with an atomic ticket);
+// "Format-aware fusion for FP4" (row-gradient stochastic rounding, fixed-sign
+// 32-point Hadamard, scale layout written for its consumer).
+//
+// Design (one kernel shape for every mode):
+//  * The tensor is cut into 128 x 128 bf16 tiles.  A persistent grid of two
+//    256-thread CTAs per SM walks the tiles; each tile arrives by two TMA
+//    loads (128 rows x 64 columns, 128-byte swizzle) into a two-stage ring,
+//    so HBM reads of the next tiles overlap the work on the current one.
+//  * Row pass: 16 lanes per row, 8 bf16 per lane; a 1x32 block is 4 lanes,
+//    its amax is two xor-shuffles.  Column pass: one lane per two columns
+//    reads 32 rows with 4-byte shared loads (conflict-free) and owns two
+//    32x1 blocks entirely in registers.
+//  * Codes are staged in shared memory and leave by TMA stores (the column
+//    copy is written transposed, so its rows are 128 contiguous bytes of
+//    the tile); scales leave as 4-byte or 16-byte stores in the requested
+//    layout (canonical, or the GEMM's 512-byte tensor-core chunks).
+//  * One HBM read of x produces every requested output.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mxq {
+
+constexpr int TILE = 128;
+constexpr int NST = 2;                      // input stages per CTA
+constexpr int THREADS = 256;
+constexpr int IN_STAGE_BYTES = TILE * TILE * 2;   // 32 KiB (two 16 KiB halves)
+constexpr int HALF_BYTES = IN_STAGE_BYTES / 2;
+
+struct QuantParams {
+  int rows, cols;
+  int tiles_c, ntiles;
+  int ceil_mode, rounding, hadamard, sf_mma;
+  uint32_t sr_k0, sr_k1, had_k0, had_k1;
+  uint8_t* s_row;
+  uint8_t* s_col;
+  int* status;
+  // per-tensor FP8
+  const float* scale;
+  float* ring;
+  int hist_len, hist_idx;
+  float fp8_max, margin;
+  float* amax_out;
+};
+
+// destmax = m_d * 2^E_d: exponent and 23-bit mantissa field of the largest
+// finite element (E4M3 1.75*2^8, E5M2 1.75*2^15, E2M1 1.5*2^2).
+template <int FMT> struct FmtInfo;
+template <> struct FmtInfo<MXQ_E4M3> { static constexpr int Ed = 8;  static constexpr uint32_t md = 0x600000u; static constexpr int mbits = 3; static constexpr int emin = -6;  static constexpr float maxv = 448.f; };
+template <> struct FmtInfo<MXQ_E5M2> { static constexpr int Ed = 15; static constexpr uint32_t md = 0x600000u; static constexpr int mbits = 2; static constexpr int emin = -14; static constexpr float maxv = 57344.f; };
+template <> struct FmtInfo<MXQ_E2M1> { static constexpr int Ed = 2;  static constexpr uint32_t md = 0x400000u; static constexpr int mbits = 1; static constexpr int emin = 0;   static constexpr float maxv = 6.f; };
+
+// Shared exponent e from the block amax given as float32 bits (>= 0, finite,
+// bf16 values are exact float32): floor rule e = E(amax) - E(destmax); ceil
+// rule adds 1 when amax's mantissa exceeds destmax's.  amax == 0 -> -127.
+template <int FMT>
+__device__ __forceinline__ int scale_exp(uint32_t ab, int ceil_mode) {
+  if (ab == 0u) return -127;
+  int E;
+  uint32_t man;
+  const uint32_t bexp = ab >> 23;
+  if (bexp == 0u) {                       // float32 subnormal
+    const int lz = __clz(ab);             // leading 1 at bit 31 - lz
+    E = (31 - lz) - 149;
+    man = (ab << (lz - 8)) & 0x7FFFFFu;
+  } else {
+    E = static_cast<int>(bexp) - 127;
+    man = ab & 0x7FFFFFu;
+  }
+  int e = E - FmtInfo<FMT>::Ed;
+  if (ceil_mode && man > FmtInfo<FMT>::md) e += 1;
+  return max(-127, min(127, e));
+}
+
+// 2^-e as float32 (e in [-127, 125] here, so the result is a normal number).
+__device__ __forceinline__ float exp2_neg(int e) {
+  return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// Stochastic rounding of y (float32, exact) to the element grid with the
+// 32-bit draw r: magnitude y' = min(|y|, max) between grid neighbours
+// lo <= y' < lo + sp rounds up iff r < floor((y' - lo) / sp * 2^32).  All
+// steps are exact in float32 (power-of-two scalings and a difference of two
+// nearby values).  Returns the rounded value (on the grid, sign kept).
+template <int FMT>
+__device__ __forceinline__ float sr_round(float y, uint32_t r) {
+  const float a = fminf(fabsf(y), FmtInfo<FMT>::maxv);
+  const int bexp = static_cast<int>(__float_as_uint(a) >> 23) - 127;
+  const int E = max(bexp, FmtInfo<FMT>::emin);
+  const float sp = __uint_as_float(static_cast<uint32_t>(E - FmtInfo<FMT>::mbits + 127) << 23);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - (E - FmtInfo<FMT>::mbits)) << 23);
+  const float n = floorf(__fmul_rn(a, inv));
+  const float lo = __fmul_rn(n, sp);
+  const float frac = __fmul_rn(__fsub_rn(a, lo), inv);          // in [0, 1), exact
+  const uint32_t t = __float2uint_rz(__fmul_rn(frac, 4294967296.0f));
+  const float mag = (r < t) ? __fadd_rn(lo, sp) : lo;
+  return copysignf(mag, y);
+}
+
+// Hadamard signs: bit j of word 0 of Philox-4x32-10(key = seed, counter = 0).
+__device__ __forceinline__ uint32_t hadamard_sign_mask(uint32_t k0, uint32_t k1) {
+  return philox4x32_10(u32x4{0u, 0u, 0u, 0u}, k0, k1).x;
+}
+
+__device__ __forceinline__ uint32_t sr_draw(uint64_t idx, uint32_t k0, uint32_t k1) {
+  return philox4x32_10(u32x4{static_cast<uint32_t>(idx), static_cast<uint32_t>(idx >> 32), 0u, 0u}, k0, k1).x;
+}
+
+constexpr float kHadC = 0.17677669529663688f;  // float32 nearest 1/sqrt(32)
+
+// In-register butterfly stages h = 1, 2, 4 over 8 consecutive block
+// positions: (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h}).
+__device__ __forceinline__ void fwht8(float* u) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float a = u[i], b = u[i + h];
+        u[i] = __fadd_rn(a, b);
+        u[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+}
+
+// Full 32-point transform of a block held by one thread (column pass).
+__device__ __forceinline__ void hadamard32_local(float* u, uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) u[j] = ((signs >> j) & 1u) ? -u[j] : u[j];
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & h) == 0) {
+        const float a = u[i], b = u[i + h];
+        u[i] = __fadd_rn(a, b);
+        u[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) u[j] = __fmul_rn(u[j], kHadC);
+}
+
+// 32-point transform of a row block spread over 4 lanes (8 values each, block
+// position = 8 * (lane & 3) + j): stages 1, 2, 4 in registers, then 8 and 16
+// across lanes (xor 1, xor 2).
+__device__ __forceinline__ void hadamard32_row(float* u, int sub, uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) u[j] = ((signs >> (sub * 8 + j)) & 1u) ? -u[j] : u[j];
+  fwht8(u);
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int bit = 1 << s;               // lane bit for h = 8 (s=0), 16 (s=1)
+    const bool upper = (sub & bit) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float other = __shfl_xor_sync(0xFFFFFFFFu, u[j], bit);
+      u[j] = upper ? __fsub_rn(other, u[j]) : __fadd_rn(u[j], other);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(u[j], kHadC);
+}
+
+__device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// Encode 8 scaled values; returns packed codes (FP8: 8 bytes, E2M1: 4 bytes in .x).
+template <int FMT>
+__device__ __forceinline__ uint2 encode8(const float* y) {
+  if constexpr (FMT == MXQ_E2M1) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
+    return make_uint2(w, 0u);
+  } else {
+    uint32_t w0 = cvt_fp8x2<FMT>(y[0], y[1]) | (cvt_fp8x2<FMT>(y[2], y[3]) << 16);
+    uint32_t w1 = cvt_fp8x2<FMT>(y[4], y[5]) | (cvt_fp8x2<FMT>(y[6], y[7]) << 16);
+    return make_uint2(w0, w1);
+  }
+}
+
+// Offsets of the scale byte of (row r, block b) of a 128 x 4 staging chunk.
+__device__ __forceinline__ int sf_stage_off(int r, int b, int mma) {
+  return mma ? ((r & 31) * 16 + ((r >> 5) & 3) * 4 + b) : (r * 4 + b);
+}
+
+// EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
+// time by the parameters); without it the kernel is the lean RNE variant.
+template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA>
+__global__ void __launch_bounds__(THREADS, 2)
+quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
+                   const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
+  constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
+  constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
+  constexpr bool FP4 = (FMT == MXQ_E2M1);
+  constexpr int QB = FP4 ? TILE / 2 : TILE;              // code bytes per tile row
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* in_s = smem;
+  uint8_t* qrow_s = in_s + NST * IN_STAGE_BYTES;
+  uint8_t* qcol_s = qrow_s + 16384;
+  uint8_t* scr_s = qcol_s + 16384;
+  uint8_t* scc_s = scr_s + 512;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scc_s + 512);
+  uint32_t* red = reinterpret_cast<uint32_t*>(bars + NST);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t signs = (EXTRA && p.hadamard) ? hadamard_sign_mask(p.had_k0, p.had_k1) : 0u;
+  const float mult = PERTENSOR ? *p.scale : 1.0f;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+    prefetch_tensormap(&map_x);
+    if (DO_ROW) prefetch_tensormap(&map_qrow);
+    if (DO_COL) prefetch_tensormap(&map_qcol);
+  }
+  __syncthreads();
+
+  int issued = 0;
+  auto issue = [&](int i) {  // thread 0 only
+    const int tile = blockIdx.x + i * gridDim.x;
+    const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
+    const uint32_t bar = smem_u32(&bars[i % NST]);
+    uint8_t* dst = in_s + (i % NST) * IN_STAGE_BYTES;
+    mbar_arrive_expect_tx(bar, IN_STAGE_BYTES);
+    tma_load_2d(smem_u32(dst), &map_x, bar, c0, r0);
+    tma_load_2d(smem_u32(dst + HALF_BYTES), &map_x, bar, c0 + 64, r0);
+  };
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      if (blockIdx.x + i * gridDim.x < p.ntiles) { issue(i); issued = i + 1; }
+    }
+  }
+
+  uint32_t amax_acc = 0;   // per-tensor: running max of |x| bits
+  bool aborted = false;
+  int i = 0;
+  for (;; ++i) {
+    const int tile = blockIdx.x + i * gridDim.x;
+    if (tile >= p.ntiles) break;
+    const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
+    const int s = i % NST;
+    const bool ok = mbar_wait(smem_u32(&bars[s]), (i / NST) & 1, p.status);
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (tid == 0) bulk_wait_read_all();     // staging buffers free again
+    __syncthreads();
+    const uint8_t* in = in_s + s * IN_STAGE_BYTES;
+
+    // ------------------------------------------------------------ row pass
+    if constexpr (DO_ROW) {
+      const int lr = lane & 15, rs = lane >> 4;
+      const int hh = lr >> 3, ch = lr & 7, sub = lr & 3;
+#pragma unroll 2
+      for (int it = warp; it < TILE / 2; it += THREADS / 32) {
+        const int r = it * 2 + rs;
+        const uint4 raw = *reinterpret_cast<const uint4*>(in + hh * HALF_BYTES + r * 128 + ((ch ^ (r & 7)) << 4));
+        float v[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
+                      bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
+        uint2 codes;
+        if constexpr (PERTENSOR) {
+          uint32_t ab = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) { ab = max(ab, absbits(v[j])); v[j] = __fmul_rn(v[j], mult); }
+          amax_acc = max(amax_acc, ab);
+          codes = encode8<FMT>(v);
+        } else {
+          if (EXTRA && p.hadamard) hadamard32_row(v, sub, signs);
+          uint32_t ab = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ab = max(ab, absbits(v[j]));
+          ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
+          ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
+          const bool bad = ab >= 0x7F800000u;
+          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
+          const float m = exp2_neg(e);
+          if (EXTRA && p.rounding == MXQ_SR) {
+            const uint64_t base = static_cast<uint64_t>(r0 + r) * static_cast<uint64_t>(p.cols) + (c0 + lr * 8);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw(base + j, p.sr_k0, p.sr_k1));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], m);
+          }
+          codes = encode8<FMT>(v);
+          if (bad) codes = make_uint2(0u, 0u);
+          if (sub == 0) scr_s[sf_stage_off(r, lr >> 2, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+        }
+        if constexpr (FP4) {
+          *reinterpret_cast<uint32_t*>(qrow_s + r * QB + lr * 4) = codes.x;
+        } else {
+          *reinterpret_cast<uint2*>(qrow_s + r * QB + lr * 8) = codes;
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ column pass
+    if constexpr (DO_COL) {
+      const int hh = warp & 1, rb = warp >> 1;
+      const int chk = lane >> 2, wb = (lane & 3) * 4;
+      uint32_t w[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int row = rb * 32 + k;
+        w[k] = *reinterpret_cast<const uint32_t*>(in + hh * HALF_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int cl = hh * 64 + 2 * lane + half;       // tile column
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = half ? bf16hi(w[k]) : bf16lo(w[k]);
+        uint32_t cw[8];
+        if constexpr (PERTENSOR) {
+          uint32_t ab = 0;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { ab = max(ab, absbits(v[k])); v[k] = __fmul_rn(v[k], mult); }
+          if (!DO_ROW) amax_acc = max(amax_acc, ab);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) cw[k] = cvt_fp8x2<FMT>(v[4 * k], v[4 * k + 1]) | (cvt_fp8x2<FMT>(v[4 * k + 2], v[4 * k + 3]) << 16);
+        } else {
+          if (EXTRA && p.hadamard) hadamard32_local(v, signs);
+          uint32_t ab = 0;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
+          const bool bad = ab >= 0x7F800000u;
+          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
+          const float m = exp2_neg(e);
+          if (EXTRA && p.rounding == MXQ_SR) {
+            const int c = c0 + cl;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const uint64_t idx = static_cast<uint64_t>(r0 + rb * 32 + k) * static_cast<uint64_t>(p.cols) + c;
+              v[k] = sr_round<FMT>(__fmul_rn(v[k], m), sr_draw(idx, p.sr_k0, p.sr_k1));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __fmul_rn(v[k], m);
+          }
+          if constexpr (FP4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t x = 0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) x |= cvt_e2m1x2(v[8 * k + 2 * j], v[8 * k + 2 * j + 1]) << (8 * j);
+              cw[k] = bad ? 0u : x;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t x = cvt_fp8x2<FMT>(v[4 * k], v[4 * k + 1]) | (cvt_fp8x2<FMT>(v[4 * k + 2], v[4 * k + 3]) << 16);
+              cw[k] = bad ? 0u : x;
+            }
+          }
+          scc_s[sf_stage_off(cl, rb, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+        }
+        if constexpr (FP4) {
+          // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (addr >> 7) & 3
+          const int phys = (rb ^ ((cl >> 1) & 3)) << 4;
+          *reinterpret_cast<uint4*>(qcol_s + cl * 64 + phys) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        } else {
+          // [128 cols][128 B], 128-byte swizzle: 16-B chunk index ^= col & 7
+          const int c7 = cl & 7;
+          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        }
+      }
+    }
+
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      if constexpr (DO_ROW) tma_store_2d(&map_qrow, smem_u32(qrow_s), FP4 ? c0 / 2 : c0, r0);
+      if constexpr (DO_COL) tma_store_2d(&map_qcol, smem_u32(qcol_s), FP4 ? r0 / 2 : r0, c0);
+      bulk_commit();
+      if (blockIdx.x + (i + NST) * gridDim.x < p.ntiles) { issue(i + NST); issued = i + NST + 1; }
+    }
+
+    // ------------------------------------------------------------ scales out
+    if constexpr (!PERTENSOR) {
+      if constexpr (DO_ROW) {
+        if (p.sf_mma) {
+          if (tid < 32) {
+            const int kb4 = p.cols / 128;
+            uint8_t* dst = p.s_row + (static_cast<size_t>(r0 / 128) * kb4 + c0 / 128) * 512;
+            reinterpret_cast<uint4*>(dst)[tid] = reinterpret_cast<const uint4*>(scr_s)[tid];
+          }
+        } else if (tid < TILE && r0 + tid < p.rows) {
+          const int kb = p.cols / 32, b0 = c0 / 32;
+          const uint32_t v = reinterpret_cast<const uint32_t*>(scr_s)[tid];
+          uint8_t* dst = p.s_row + static_cast<size_t>(r0 + tid) * kb + b0;
+          if ((kb & 3) == 0 && b0 + 4 <= kb) {
+            *reinterpret_cast<uint32_t*>(dst) = v;
+          } else {
+            for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+          }
+        }
+      }
+      if constexpr (DO_COL) {
+        if (p.sf_mma) {
+          if (tid < 32) {
+            const int rb4 = p.rows / 128;
+            uint8_t* dst = p.s_col + (static_cast<size_t>(c0 / 128) * rb4 + r0 / 128) * 512;
+            reinterpret_cast<uint4*>(dst)[tid] = reinterpret_cast<const uint4*>(scc_s)[tid];
+          }
+        } else if (tid < TILE && c0 + tid < p.cols) {
+          const int kb = p.rows / 32, b0 = r0 / 32;
+          const uint32_t v = reinterpret_cast<const uint32_t*>(scc_s)[tid];
+          uint8_t* dst = p.s_col + static_cast<size_t>(c0 + tid) * kb + b0;
+          if ((kb & 3) == 0 && b0 + 4 <= kb) {
+            *reinterpret_cast<uint32_t*>(dst) = v;
+          } else {
+            for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (tid == 0) {
+    bulk_wait_all();
+    if (aborted) {
+      for (int j = i; j < issued; ++j) (void)mbar_wait(smem_u32(&bars[j % NST]), (j / NST) & 1, p.status);
+    }
+  }
+
+  if constexpr (PERTENSOR) {
+    // block amax -> the ring's amax slot or amax_out; last block folds.
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
+    if (lane == 0) red[warp] = amax_acc;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t m = 0;
+      for (int k = 0; k < THREADS / 32; ++k) m = max(m, red[k]);
+      const int n = p.hist_len;
+      if (p.ring == nullptr) {
+        atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), m);
+      } else {
+        float* ring = p.ring;
+        atomicMax(reinterpret_cast<unsigned int*>(ring + n + 2), m);
+        __threadfence();
+        const unsigned int ticket = atomicAdd(reinterpret_cast<unsigned int*>(ring + n + 3), 1u);
+        if (ticket == gridDim.x - 1) {
+          __threadfence();
+          volatile float* vr = ring;
+          const float amax = vr[n + 2];
+          vr[p.hist_idx] = amax;
+          float M = vr[0];
+          for (int k = 1; k < n; ++k) {
+            const float a = vr[k];
+            if (isnan(a) || a > M) M = a;
+          }
+          if (M > 0.f && isfinite(M)) {
+            const float sc = __fdiv_rn(__fdiv_rn(M, p.fp8_max), p.margin);
+            vr[n] = sc;
+            vr[n + 1] = __frcp_rn(sc);
+          }
+          if (p.amax_out) *p.amax_out = amax;
+          vr[n + 2] = 0.f;
+          reinterpret_cast<volatile unsigned int*>(ring)[n + 3] = 0u;
+          __threadfence();
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dequantize
+template <int FMT>
+__global__ void dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows,
+                               int64_t cols, int out_fp32, void* __restrict__ out) {
+  // one thread: 16 consecutive elements of one row (inside one 32-block)
+  const int64_t groups = rows * (cols / 16);
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / (cols / 16), c = (g % (cols / 16)) * 16;
+    const uint8_t sc = s[r * (cols / 32) + c / 32];
+    const float X = (sc == 0xFF) ? __uint_as_float(0x7FC00000u)
+                   : (sc == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(sc) << 23));
+    float v[16];
+    if constexpr (FMT == MXQ_E2M1) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(q + r * (cols / 2) + c / 2);
+      const uint32_t wds[2] = {raw.x, raw.y};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint16_t b = static_cast<uint16_t>((wds[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+        uint32_t h2;
+        asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(b));
+        v[2 * k] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+        v[2 * k + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+      }
+    } else {
+      const uint4 raw = *reinterpret_cast<const uint4*>(q + r * cols + c);
+      const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint16_t b = static_cast<uint16_t>((wds[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
+        uint32_t h2;
+        if constexpr (FMT == MXQ_E4M3) {
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+        } else {
+          asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(b));
+        }
+        v[2 * k] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+        v[2 * k + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], X);
+    if (out_fp32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + r * cols + c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    } else {
+      uint32_t b[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k]));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k + 1]));
+        b[k] = lo | (hi << 16);
+      }
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + r * cols + c);
+      o[0] = make_uint4(b[0], b[1], b[2], b[3]);
+      o[1] = make_uint4(b[4], b[5], b[6], b[7]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- SF layout
+__global__ void sf_to_mma_kernel(const uint8_t* __restrict__ s, int64_t rows, int64_t kb, uint8_t* __restrict__ out) {
+  // one thread: the 4 scales of one row inside one 128-K chunk
+  const int64_t n = rows * (kb / 4);
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < n;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / (kb / 4), kc = g % (kb / 4);
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(s + r * kb + kc * 4);
+    const int64_t off = ((r / 128) * (kb / 4) + kc) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4;
+    *reinterpret_cast<uint32_t*>(out + off) = v;
+  }
+}
+
+}  // namespace mxq
+
+// ==================================================================== host
+using namespace mxq;
+using namespace mxq_host;
+
+namespace {
+
+template <int FMT, int ORIENT, bool PT, bool EXTRA>
+int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
+                 cudaStream_t st) {
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA>;
+  const int smem = NST * IN_STAGE_BYTES + 16384 * 2 + 512 * 2 + 64 + 1024;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return MXQ_ERR_CUDA;
+    attr_set[dev & 63] = true;
+  }
+  const int grid = std::min(p.ntiles, 2 * sm_count());
+  kern<<<grid, THREADS, smem, st>>>(mx, mr, mc, p);
+  return launch_status();
+}
+
+template <bool PT>
+int dispatch(int fmt, int orient, const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc,
+             const QuantParams& p, cudaStream_t st) {
+  const bool extra = !PT && (p.rounding == MXQ_SR || p.hadamard);
+#define MXQ_CASE(F, O)                                                                  \
+  if (fmt == F && orient == O)                                                          \
+    return extra ? launch_tiles<F, O, PT, !PT>(mx, mr, mc, p, st)                      \
+                 : launch_tiles<F, O, PT, false>(mx, mr, mc, p, st);
+  MXQ_CASE(MXQ_E4M3, MXQ_ROW) MXQ_CASE(MXQ_E4M3, MXQ_COL) MXQ_CASE(MXQ_E4M3, MXQ_DUAL)
+  MXQ_CASE(MXQ_E5M2, MXQ_ROW) MXQ_CASE(MXQ_E5M2, MXQ_COL) MXQ_CASE(MXQ_E5M2, MXQ_DUAL)
+  if constexpr (!PT) {
+    MXQ_CASE(MXQ_E2M1, MXQ_ROW) MXQ_CASE(MXQ_E2M1, MXQ_COL) MXQ_CASE(MXQ_E2M1, MXQ_DUAL)
+  }
+#undef MXQ_CASE
+  return MXQ_ERR_UNSUPPORTED;
+}
+
+bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E5M2 || f == MXQ_E2M1; }
+bool valid_orient(int o) { return o == MXQ_ROW || o == MXQ_COL || o == MXQ_DUAL; }
+
+// Tensor maps of the tile kernel: input halves, row codes, transposed codes.
+int make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, bool fp4, int orient, void* q_row,
+              void* q_col, CUtensorMap* mx, CUtensorMap* mr, CUtensorMap* mc) {
+  if (!encode_2d(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, cols, rows, ld * 2, 64, TILE,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXQ_ERR_CUDA;
+  const int qb = fp4 ? 64 : 128;
+  *mr = *mx;
+  *mc = *mx;
+  if (orient & MXQ_ROW) {
+    const uint64_t inner = fp4 ? cols / 2 : cols;
+    if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qb, TILE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MXQ_ERR_CUDA;
+  }
+  if (orient & MXQ_COL) {
+    const uint64_t inner = fp4 ? rows / 2 : rows;
+    if (!encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, inner, cols, inner, qb, TILE,
+                   fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+      return MXQ_ERR_CUDA;
+  }
+  return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int orient,
+                            int scale_mode, int rounding, int hadamard32, uint64_t sr_key,
+                            uint64_t hadamard_seed, int sf_layout, void* q_row, uint8_t* s_row, void* q_col,
+                            uint8_t* s_col, void* stream) {
+  if (!x || !valid_fmt(fmt) || !valid_orient(orient)) return MXQ_ERR_BAD_ARG;
+  if (scale_mode != MXQ_SCALE_FLOOR_OCP && scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
+  if (rounding != MXQ_RNE && rounding != MXQ_SR) return MXQ_ERR_BAD_ARG;
+  if (sf_layout != MXQ_SF_CANONICAL && sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
+  if ((orient & MXQ_ROW) && (!q_row || !s_row)) return MXQ_ERR_BAD_ARG;
+  if ((orient & MXQ_COL) && (!q_col || !s_col)) return MXQ_ERR_BAD_ARG;
+  if (rows <= 0 || cols <= 0 || rows % 32 || cols % 32 || ld < cols) return MXQ_ERR_BAD_SHAPE;
+  if (rows > (1ll << 31) - TILE || cols > (1ll << 31) - TILE) return MXQ_ERR_BAD_SHAPE;
+  if (sf_layout == MXQ_SF_MMA && (rows % 128 || cols % 128)) return MXQ_ERR_BAD_SHAPE;
+  if (!aligned16(x) || ld % 8) return MXQ_ERR_MISALIGNED;
+  if ((orient & MXQ_ROW) && !aligned16(q_row)) return MXQ_ERR_MISALIGNED;
+  if ((orient & MXQ_COL) && !aligned16(q_col)) return MXQ_ERR_MISALIGNED;
+  if (sf_layout == MXQ_SF_MMA && (((orient & MXQ_ROW) && !aligned16(s_row)) || ((orient & MXQ_COL) && !aligned16(s_col))))
+    return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+
+  CUtensorMap mx, mr, mc;
+  int rc = make_maps(x, rows, cols, ld, fmt == MXQ_E2M1, orient, q_row, q_col, &mx, &mr, &mc);
+  if (rc) return rc;
+  QuantParams p{};
+  p.rows = static_cast<int>(rows);
+  p.cols = static_cast<int>(cols);
+  p.tiles_c = static_cast<int>((cols + TILE - 1) / TILE);
+  p.ntiles = p.tiles_c * static_cast<int>((rows + TILE - 1) / TILE);
+  p.ceil_mode = scale_mode == MXQ_SCALE_CEIL;
+  p.rounding = rounding;
+  p.hadamard = hadamard32 != 0;
+  p.sf_mma = sf_layout == MXQ_SF_MMA;
+  p.sr_k0 = static_cast<uint32_t>(sr_key);
+  p.sr_k1 = static_cast<uint32_t>(sr_key >> 32);
+  p.had_k0 = static_cast<uint32_t>(hadamard_seed);
+  p.had_k1 = static_cast<uint32_t>(hadamard_seed >> 32);
+  p.s_row = s_row;
+  p.s_col = s_col;
+  p.status = status_ptr();
+  if (!p.status) return MXQ_ERR_CUDA;
+  return dispatch<false>(fmt, orient, mx, mr, mc, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols, const float* scale, int fmt,
+                                      int orient, float* ring_state, int hist_len, int hist_idx, float fp8_max,
+                                      float pow2_margin, uint8_t* x8, uint8_t* x8T, float* amax_out,
+                                      void* stream) {
+  if (!x || !scale || (fmt != MXQ_E4M3 && fmt != MXQ_E5M2) || !valid_orient(orient)) return MXQ_ERR_BAD_ARG;
+  if ((orient & MXQ_ROW) && !x8) return MXQ_ERR_BAD_ARG;
+  if ((orient & MXQ_COL) && !x8T) return MXQ_ERR_BAD_ARG;
+  if (!ring_state && !amax_out) return MXQ_ERR_BAD_ARG;
+  if (ring_state && (hist_len < 1 || hist_idx < 0 || hist_idx >= hist_len)) return MXQ_ERR_BAD_ARG;
+  if (rows <= 0 || cols <= 0 || cols % 16) return MXQ_ERR_BAD_SHAPE;
+  if ((orient & MXQ_COL) && rows % 16) return MXQ_ERR_BAD_SHAPE;
+  if (rows > (1ll << 31) - TILE || cols > (1ll << 31) - TILE) return MXQ_ERR_BAD_SHAPE;
+  if (!aligned16(x) || ((orient & MXQ_ROW) && !aligned16(x8)) || ((orient & MXQ_COL) && !aligned16(x8T)))
+    return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap mx, mr, mc;
+  int rc = make_maps(x, rows, cols, cols, false, orient, x8, x8T, &mx, &mr, &mc);
+  if (rc) return rc;
+  QuantParams p{};
+  p.rows = static_cast<int>(rows);
+  p.cols = static_cast<int>(cols);
+  p.tiles_c = static_cast<int>((cols + TILE - 1) / TILE);
+  p.ntiles = p.tiles_c * static_cast<int>((rows + TILE - 1) / TILE);
+  p.status = status_ptr();
+  if (!p.status) return MXQ_ERR_CUDA;
+  p.scale = scale;
+  p.ring = ring_state;
+  p.hist_len = hist_len;
+  p.hist_idx = hist_idx;
+  p.fp8_max = fp8_max;
+  p.margin = pow2_margin;
+  p.amax_out = amax_out;
+  if (!ring_state) {
+    if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MXQ_ERR_CUDA;
+  }
+  return dispatch<true>(fmt, orient, mx, mr, mc, p, st);
+}
+
+extern "C" int mxq_dequantize(const void* q, const uint8_t* s, int64_t rows, int64_t cols, int fmt, int out_fp32,
+                              void* out, void* stream) {
+  if (!q || !s || !out || !valid_fmt(fmt)) return MXQ_ERR_BAD_ARG;
+  if (rows <= 0 || cols <= 0 || cols % 32) return MXQ_ERR_BAD_SHAPE;
+  if (!aligned16(q) || !aligned16(out)) return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  const int64_t groups = rows * (cols / 16);
+  const int grid = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 8ll * sm_count()));
+  auto st = static_cast<cudaStream_t>(stream);
+  const uint8_t* qb = static_cast<const uint8_t*>(q);
+  if (fmt == MXQ_E4M3) dequant_kernel<MXQ_E4M3><<<grid, 256, 0, st>>>(qb, s, rows, cols, out_fp32, out);
+  else if (fmt == MXQ_E5M2) dequant_kernel<MXQ_E5M2><<<grid, 256, 0, st>>>(qb, s, rows, cols, out_fp32, out);
+  else dequant_kernel<MXQ_E2M1><<<grid, 256, 0, st>>>(qb, s, rows, cols, out_fp32, out);
+  return launch_status();
+}
+
+extern "C" int mxq_sf_to_mma(const uint8_t* s, int64_t rows, int64_t kb, uint8_t* out, void* stream) {
+  if (!s || !out) return MXQ_ERR_BAD_ARG;
+  if (rows <= 0 || kb <= 0 || rows % 128 || kb % 4) return MXQ_ERR_BAD_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(s) & 3) || (reinterpret_cast<uintptr_t>(out) & 3)) return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  const int64_t n = rows * (kb / 4);
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 8ll * sm_count()));
+  sf_to_mma_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(s, rows, kb, out);
+  return launch_status();
+}

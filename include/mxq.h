@@ -1,0 +1,188 @@
+/*
+ * mxq.h -- block-scaled (OCP MX) and per-tensor FP8 quantization of bf16
+ * tensors, and the block-scaled GEMM that consumes them, on NVIDIA GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, int status codes, no
+ * exceptions.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates or frees device memory; it keeps only a per-device
+ *    cache of the SM count and a device status word.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Nothing is read back to the host.
+ *  - Matrices are row-major.  "rows x cols" means cols is the contiguous
+ *    dimension.
+ *  - Element codes: one byte per FP8 element; E2M1 is packed two per byte,
+ *    element 2i in the low nibble and 2i+1 in the high nibble.
+ *  - Scale codes are UE8M0 bytes: code c means 2^(c-127); 0xFF is NaN.
+ *  - Return value: MXQ_OK or a negative status (see mxq_strerror).  Argument
+ *    checks happen before any launch; on error nothing is launched.
+ *
+ * Sources of the operations (page title, section):
+ *  [MX]  "UE8M0 FP8 / MXFP8 explainer" (ag-981.com), section 1 (MX block of
+ *        k = 32 elements sharing one UE8M0 scale X; quantizing V_i means
+ *        finding X and q_i with q_i * X ~= V_i; tensor cores consume X and
+ *        q_i of both operands), section 4 (scale from the block amax,
+ *        saturating element quantization), gap section 1 (OCP round-down
+ *        versus ceil(log2(amax/destmax)) scales), gap section 2 (row and
+ *        column copies; blocks must run along the contiguous reduction
+ *        dimension).
+ *  [FP8] AstrAI astrai/extension/ops/fp8.py (commit 962c10c52b): commit
+ *        message (last-block delayed-scaling fold with an atomic ticket) and
+ *        the quantize / quantize_dual docstrings.
+ *  [FAF] "Format-aware fusion for FP4" (theaicronicle.com): MXFP4 with
+ *        row-gradient stochastic rounding and a fixed-sign 32-point
+ *        Hadamard; producers emit the scale layout their consumer reads.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define MXQ_OK               0
+#define MXQ_ERR_BAD_ARG     -1  /* NULL pointer, bad enum, bad ring index   */
+#define MXQ_ERR_BAD_SHAPE   -2  /* size not a multiple of the block/tile    */
+#define MXQ_ERR_MISALIGNED  -3  /* pointer or leading dimension not 16-B    */
+#define MXQ_ERR_UNSUPPORTED -4  /* format/orientation combination, or GPU  */
+#define MXQ_ERR_CUDA        -5  /* launch or driver error                   */
+#define MXQ_ERR_TIMEOUT     -6  /* a bounded device wait expired            */
+
+/* ---- enums ---------------------------------------------------------------- */
+/* Element formats.  0/1 keep the E4M3/E5M2 numbering of [FP8] (_FMT_TO_INT). */
+#define MXQ_E4M3 0
+#define MXQ_E5M2 1
+#define MXQ_E2M1 2
+/* Orientation.  ROW: 1x32 blocks along cols, output q_row [rows][cols].
+ * COL: 32x1 blocks along rows, output stored transposed, q_col [cols][rows]
+ * (the K-contiguous copy [MX] gap section 2 asks for).  DUAL: both from one
+ * read of x. */
+#define MXQ_ROW  1
+#define MXQ_COL  2
+#define MXQ_DUAL 3
+/* Scale rule [MX] gap section 1.
+ * FLOOR_OCP: e = floor(log2 amax) - floor(log2 destmax).
+ * CEIL:      e = ceil(log2(amax / destmax)), computed from exponent and
+ *            mantissa bits (never saturates).
+ * Both: amax == 0 -> e = -127; e clamped to [-127, 127]; a block holding
+ * NaN/Inf gets scale 0xFF and zero codes. */
+#define MXQ_SCALE_FLOOR_OCP 0
+#define MXQ_SCALE_CEIL      1
+/* Element rounding.  RNE: round to nearest, ties to even code, saturating
+ * at the format maximum, sign kept on zero.  SR: stochastic rounding with
+ * r = word 0 of Philox-4x32-10(key = sr_key, counter = (i, i >> 32, 0, 0)),
+ * i = r*cols + c the element's index in x; with y' = min(|y|, max) between
+ * grid neighbours lo < y' < hi, round up iff r < floor((y'-lo)/(hi-lo)*2^32). */
+#define MXQ_RNE 0
+#define MXQ_SR  1
+/* Scale-factor layout.
+ * CANONICAL: row-major bytes, s_row [rows][cols/32], s_col [cols][rows/32].
+ * MMA: the layout the GEMM's tensor-core scale path reads ([FAF]: the
+ * producer writes its consumer's layout).  For a scale matrix of R rows and
+ * KB = K/32 scale columns (R % 128 == 0, KB % 4 == 0): 512-byte chunks, chunk
+ * (R/128 index rb, KB/4 index kc) at byte offset (rb*(KB/4) + kc)*512, and
+ * inside a chunk the scale of row r and k-block k at byte
+ * (r%32)*16 + ((r/32)%4)*4 + (k%4).  Same bytes, permuted. */
+#define MXQ_SF_CANONICAL 0
+#define MXQ_SF_MMA       1
+
+/* ---- MX quantize ([MX] sections 1 and 4, gap sections 1-2; [FAF]) ----------
+ * x        bf16 [rows][ld] (only the first cols of each row are read),
+ *          16-byte aligned, ld % 8 == 0, ld >= cols.
+ * rows, cols  multiples of 32 (rows % 128 and cols % 128 for SF_MMA;
+ *          cols % 2... E2M1 needs even counts along the packed axis, given).
+ * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1.
+ * orient   MXQ_ROW | MXQ_COL | MXQ_DUAL.
+ * scale_mode  MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL.
+ * rounding MXQ_RNE | MXQ_SR.
+ * hadamard32  non-zero: before scale selection each 32-block (along its
+ *          block direction) becomes y = c * H32 * D * v in float32: D holds
+ *          the 32 signs given by bit j of word 0 of
+ *          Philox-4x32-10(key = hadamard_seed, counter = 0) (set bit = -1),
+ *          butterflies h = 1,2,4,8,16 in that order, c = RN32(1/sqrt(32)).
+ * q_row, s_row  outputs for ROW/DUAL (else may be NULL): q_row
+ *          [rows][cols] bytes (E2M1: [rows][cols/2]); s_row per sf_layout.
+ * q_col, s_col  outputs for COL/DUAL: q_col [cols][rows] (E2M1:
+ *          [cols][rows/2]); s_col per sf_layout.
+ * All output pointers 16-byte aligned.  Outputs must not overlap x. */
+int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                 int fmt, int orient, int scale_mode, int rounding,
+                 int hadamard32, uint64_t sr_key, uint64_t hadamard_seed,
+                 int sf_layout, void* q_row, uint8_t* s_row, void* q_col,
+                 uint8_t* s_col, void* stream);
+
+/* ---- MX dequantize ([MX] section 1: V_i ~= q_i * X) --------------------------
+ * q        codes [rows][cols] (E2M1 packed [rows][cols/2]), s canonical
+ *          scales [rows][cols/32].  out [rows][cols]: float32 when
+ *          out_fp32 != 0 (exact product, overflow to Inf), else bf16 (RNE).
+ * rows >= 1, cols % 32 == 0. */
+int mxq_dequantize(const void* q, const uint8_t* s, int64_t rows, int64_t cols,
+                   int fmt, int out_fp32, void* out, void* stream);
+
+/* ---- per-tensor FP8 quantize with fused amax and delayed-scaling fold ([FP8])
+ * x        bf16 [rows][cols], 16-byte aligned, cols % 8 == 0.  For COL/DUAL
+ *          rows % 16 == 0 and cols % 16 == 0.
+ * scale    device float: the quantization multiplier m; x8 = RNE-saturating
+ *          FP8 of RN32(x * m).  May alias ring_state[hist_len + 1].
+ * fmt      MXQ_E4M3 | MXQ_E5M2.
+ * orient   MXQ_ROW -> x8 [rows][cols]; MXQ_COL -> x8T [cols][rows] only
+ *          ([FP8] transposed=True); MXQ_DUAL -> both from one read.
+ * ring_state  NULL, or device float[hist_len + 4] laid out
+ *          [hist[hist_len] | scale | legacy | amax | done]; amax and done
+ *          must be 0 on entry (the kernel leaves them 0).  The last block
+ *          to finish folds the tensor amax into hist[hist_idx] and, if
+ *          M = max(hist) is finite and > 0, publishes
+ *          scale = RN32(RN32(M / fp8_max) / pow2_margin) and
+ *          legacy = RN32(1 / scale) (the next step's multiplier).
+ * amax_out NULL or device float: receives max|x| (without a ring it is
+ *          zeroed on the stream first, so it must not alias x or outputs).
+ *          At least one of ring_state / amax_out must be given.
+ * Concurrent calls sharing a ring_state race; calls on one stream are
+ * ordered. */
+int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
+                           const float* scale, int fmt, int orient,
+                           float* ring_state, int hist_len, int hist_idx,
+                           float fp8_max, float pow2_margin, uint8_t* x8,
+                           uint8_t* x8T, float* amax_out, void* stream);
+
+/* ---- block-scaled GEMM ([MX] section 1: tensor cores consume X and q_i of
+ * both operands, FP32 accumulation) -------------------------------------------
+ * C[m][n] = sum_k dec(a[m][k]) * 2^(sa[m][k/32]-127) * dec(b[n][k]) *
+ *           2^(sb[n][k/32]-127), accumulated in float32 on the tensor cores,
+ * written as bf16 (RNE) or, with out_fp32 != 0, float32.
+ * a_q [M][K] codes, b_q [N][K] codes (both K-contiguous; E2M1 packed
+ *          [M][K/2], [N][K/2]); a_s, b_s scales in MXQ_SF_MMA layout.
+ * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1 (same for both operands).
+ * M % 128 == 0, N % 128 == 0, K % 128 == 0 (E2M1: K % 256 == 0).
+ * c [M][N], 16-byte aligned. */
+int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q,
+             const uint8_t* b_s, int64_t M, int64_t N, int64_t K, int fmt,
+             int sf_layout, void* c, int out_fp32, void* stream);
+
+/* ---- scale layout conversion ([FAF]) -----------------------------------------
+ * Canonical scales s [rows][kb] -> MMA layout (rows % 128 == 0,
+ * kb % 4 == 0).  out holds rows*kb bytes; must not overlap s. */
+int mxq_sf_to_mma(const uint8_t* s, int64_t rows, int64_t kb, uint8_t* out,
+                  void* stream);
+
+/* ---- diagnostics ----------------------------------------------------------
+ * mxq_last_device_status: synchronizes `stream`, returns MXQ_ERR_TIMEOUT if
+ * any kernel of this library on the current device gave up a bounded wait
+ * since the last call (then clears the word), MXQ_ERR_CUDA on a CUDA error,
+ * else MXQ_OK. */
+int mxq_last_device_status(void* stream);
+const char* mxq_strerror(int status);
+/* Library version, major*10000 + minor*100 + patch. */
+int mxq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -166,7 +166,8 @@ def stochastic_round(f, y: np.ndarray, r: np.ndarray) -> np.ndarray:
 # ------------------------------------------------------------------ tensor quantizer
 def quantize(x: np.ndarray, f, orient: int = ROW, mode: int = FLOOR,
              rounding: int = RNE, hadamard32: bool = False,
-             sr_seed: int = 0, hadamard_seed: int = 7):
+             sr_seed: int = 0, hadamard_seed: int = 7,
+             row_index=None, total_cols: int | None = None):
     """MX-quantize a 2-D tensor ``x`` (float64 holding exact bf16 values).
 
     Row orientation: blocks x[r, 32j:32j+32]; codes q_row [R][C] and scales
@@ -174,6 +175,10 @@ def quantize(x: np.ndarray, f, orient: int = ROW, mode: int = FLOOR,
     stored transposed, codes q_col [C][R] and scales s_col [C][R/32], so that
     q_col is the row-wise quantization of x^T.  E2M1 codes are packed two per
     byte (low nibble = even index along the contiguous axis).
+
+    ``row_index`` / ``total_cols`` let a caller quantize sampled rows of a
+    larger tensor: element (i, c) then has flat index
+    row_index[i] * total_cols + c (the stochastic-rounding counter).
 
     Returns a dict with the requested outputs."""
     f = F.fmt(f)
@@ -184,19 +189,27 @@ def quantize(x: np.ndarray, f, orient: int = ROW, mode: int = FLOOR,
     if orient in (COL, DUAL):
         assert R % K == 0
     out = {}
-    idx = np.arange(R * C, dtype=np.int64).reshape(R, C)
+    if row_index is None:
+        idx = np.arange(R * C, dtype=np.int64).reshape(R, C)
+    else:
+        tc = C if total_cols is None else int(total_cols)
+        idx = np.asarray(row_index, dtype=np.int64)[:, None] * tc + np.arange(C, dtype=np.int64)[None, :]
 
     def one(xx, ii):
         rr, cc = xx.shape
-        vb = xx.reshape(rr, cc // K, K)
-        ib = ii.reshape(rr, cc // K, K)
-        if hadamard32:
-            vb = hadamard32_blocks(rn32(vb), hadamard_seed).astype(np.float64)
-        q, s = quantize_blocks(vb, f, mode, rounding, sr_seed, ib)
-        q = q.reshape(rr, cc)
-        if f.nbits == 4:
-            q = F.pack_fp4(q)
-        return q, s
+        qs, ss = [], []
+        for a in range(0, rr, 512):          # row slices bound the temporaries
+            vb = xx[a:a + 512].reshape(-1, cc // K, K)
+            ib = ii[a:a + 512].reshape(-1, cc // K, K)
+            if hadamard32:
+                vb = hadamard32_blocks(rn32(vb), hadamard_seed).astype(np.float64)
+            q, s = quantize_blocks(vb, f, mode, rounding, sr_seed, ib)
+            q = q.reshape(-1, cc)
+            if f.nbits == 4:
+                q = F.pack_fp4(q)
+            qs.append(q)
+            ss.append(s)
+        return np.concatenate(qs), np.concatenate(ss)
 
     if orient in (ROW, DUAL):
         out["q_row"], out["s_row"] = one(x, idx)

@@ -1,0 +1,106 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point that
+include/*.h declares, and rejects bad arguments before touching a GPU.
+CPU only: no call here launches a kernel."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    import block_scaled_precision_02_gb300 as mxq
+    from block_scaled_precision_02_gb300 import build
+    if not os.path.exists(mxq.LIB_PATH):
+        build.build()
+    return mxq.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_sf_to_mma",
+              "mxq_last_device_status", "mxq_strerror", "mxq_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(so):
+    for n in declared_functions():
+        assert hasattr(so, n), n
+
+
+def test_strerror_and_version(so):
+    for code in range(0, -7, -1):
+        assert so.mxq_strerror(code)
+    assert so.mxq_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)           # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)
+
+
+def test_argument_checks_need_no_gpu(so):
+    q = so.mxq_quantize
+    # NULL input, bad format / orientation / scale mode / rounding / layout
+    assert q(None, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 9, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 0, 4, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 0, 1, 2, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 0, 1, 0, 2, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 5, FAKE, FAKE, None, None, None) == -1
+    # missing column outputs for DUAL
+    assert q(FAKE, 64, 64, 64, 0, 3, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    # shapes: not multiples of 32, ld < cols, MMA layout needs multiples of 128
+    assert q(FAKE, 48, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
+    assert q(FAKE, 64, 64, 32, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
+    assert q(FAKE, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 1, FAKE, FAKE, None, None, None) == -2
+    # misaligned input or leading dimension
+    assert q(ODD, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -3
+    assert q(FAKE, 64, 64, 68, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -3
+
+    p = so.fp8_quantize_pertensor
+    assert p(FAKE, 64, 64, FAKE, 2, 1, None, 0, 0, 448.0, 1.0, FAKE, None, FAKE, None) == -1   # E2M1
+    assert p(FAKE, 64, 64, FAKE, 0, 1, None, 0, 0, 448.0, 1.0, FAKE, None, None, None) == -1   # no amax sink
+    assert p(FAKE, 64, 64, FAKE, 0, 1, FAKE, 16, 16, 448.0, 1.0, FAKE, None, None, None) == -1 # hist_idx
+    assert p(FAKE, 64, 40, FAKE, 0, 1, None, 0, 0, 448.0, 1.0, FAKE, None, FAKE, None) == -2
+    assert p(FAKE, 40, 64, FAKE, 0, 3, None, 0, 0, 448.0, 1.0, FAKE, FAKE, FAKE, None) == -2
+
+    g = so.mxq_gemm
+    assert g(None, FAKE, FAKE, FAKE, 128, 128, 128, 0, 1, FAKE, 0, None) == -1
+    assert g(FAKE, FAKE, FAKE, FAKE, 128, 128, 128, 0, 0, FAKE, 0, None) == -4   # canonical scales
+    assert g(FAKE, FAKE, FAKE, FAKE, 100, 128, 128, 0, 1, FAKE, 0, None) == -2
+    assert g(FAKE, FAKE, FAKE, FAKE, 128, 128, 128, 2, 1, FAKE, 0, None) == -2   # E2M1 needs K % 256
+    assert g(ODD, FAKE, FAKE, FAKE, 128, 128, 128, 0, 1, FAKE, 0, None) == -3
+
+    assert so.mxq_dequantize(FAKE, FAKE, 64, 48, 0, 1, FAKE, None) == -2
+    assert so.mxq_sf_to_mma(FAKE, 100, 4, FAKE, None) == -2
+
+
+def test_package_has_no_fallback(monkeypatch, tmp_path):
+    """Without the built library every entry point raises (no CPU path)."""
+    import block_scaled_precision_02_gb300 as mxq
+    monkeypatch.setattr(mxq, "_lib", None)
+    monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        mxq.load()
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "block_scaled_precision_02_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            text = open(path).read()
+            assert "import oracle" not in text and "from oracle" not in text, path

@@ -1,0 +1,130 @@
+"""GPU parity of the block-scaled GEMM against the oracle's float64 product.
+
+Operands are quantized by the CPU oracle (never by the CUDA path), their
+scales permuted into the tensor-core layout by the oracle, then multiplied
+on the GPU.  Structured cases whose result is exactly representable must
+match bit for bit; general cases must pass the 2e-3 gate (oracle.gemm).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_02_gb300 import inputs
+from oracle import formats as F
+from oracle import gemm as og
+from oracle import mx as omx
+from tests.helpers import f64
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2, "e2m1": F.E2M1}
+TOL = 2e-3
+
+
+def oracle_operand(x_f64, fmt, mode=omx.FLOOR):
+    r = omx.quantize(x_f64, FMTS[fmt], omx.ROW, mode)
+    return r["q_row"], r["s_row"]
+
+
+def gpu_gemm(lib, aq, as_, bq, bs, fmt, out_dtype=torch.bfloat16):
+    dev = torch.device("cuda")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    c = lib.mx_gemm(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt, out_dtype)
+    return c.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+def test_unit_rows_select_columns_exactly(lib, fmt):
+    """B row n holds a single non-zero at column perm[n]: C[:, n] is a scaled
+    copy of one dequantized column of A (exact in bf16), so the scale mapping
+    of both operands is checked bit for bit."""
+    f = FMTS[fmt]
+    rng = np.random.default_rng(1)
+    M, N, K = 128, 256, 512
+    a = rng.standard_normal((M, K)) * np.exp2(rng.integers(-6, 6, size=(M, K // 32))).repeat(32, 1)
+    aq, as_ = oracle_operand(a, fmt)
+    perm = rng.permutation(K)[:N]
+    b = np.zeros((N, K))
+    b[np.arange(N), perm] = np.exp2(rng.integers(-3, 4, size=N)) * (1.5 if fmt != "e2m1" else 1.0)
+    bq, bs = oracle_operand(b, fmt)
+    ref = og.reference(aq, as_, bq, bs, f)
+    got = gpu_gemm(lib, aq, as_, bq, bs, fmt)
+    assert np.array_equal(got, ref), f"max abs diff {np.max(np.abs(got - ref))}"
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 1024), (384, 384, 512), (128, 128, 2048)])
+def test_random_gemm_gate(lib, fmt, mnk):
+    M, N, K = mnk
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = oracle_operand(a, fmt)
+    bq, bs = oracle_operand(b, fmt)
+    ref = og.reference(aq, as_, bq, bs, FMTS[fmt])
+    got = gpu_gemm(lib, aq, as_, bq, bs, fmt)
+    err = og.gate_error(got, ref)
+    assert err <= TOL, (err, og.frobenius_rel(got, ref))
+
+
+def test_fp32_output_and_many_tiles(lib):
+    """float32 epilogue, and more output tiles than SMs (the persistent loop)."""
+    M, N, K = 2048, 4096, 256
+    a = f64(inputs.activations(M, K, seed=5))
+    b = f64(inputs.weights(N, K, seed=6))
+    aq, as_ = oracle_operand(a, "e4m3", omx.CEIL)
+    bq, bs = oracle_operand(b, "e4m3", omx.CEIL)
+    ref = og.reference(aq, as_, bq, bs, F.E4M3)
+    got32 = gpu_gemm(lib, aq, as_, bq, bs, "e4m3", torch.float32)
+    assert og.gate_error(got32, ref, out_is_bf16=False) <= 1e-5
+    got16 = gpu_gemm(lib, aq, as_, bq, bs, "e4m3")
+    assert og.gate_error(got16, ref) <= TOL
+
+
+def test_pm_one_operands_integer_sums(lib):
+    """All-+-1 E2M1 operands: every product and partial sum is a small
+    integer, exact in float32, so C equals a @ b^T exactly."""
+    rng = np.random.default_rng(2)
+    M, N, K = 256, 256, 512
+    a = rng.choice([-1.0, 1.0], (M, K))
+    b = rng.choice([-1.0, 1.0], (N, K))
+    aq, as_ = oracle_operand(a, "e2m1")
+    bq, bs = oracle_operand(b, "e2m1")
+    got = gpu_gemm(lib, aq, as_, bq, bs, "e2m1", torch.float32)
+    assert np.array_equal(got, a @ b.T)
+
+
+def _sampled(lib, M, N, K, fmt, gen_a, gen_b, nrows=64, ncols=64):
+    a = f64(gen_a(M, K))
+    b = f64(gen_b(N, K))
+    aq, as_ = oracle_operand(a, fmt)
+    bq, bs = oracle_operand(b, fmt)
+    got = gpu_gemm(lib, aq, as_, bq, bs, fmt)
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(M, nrows, replace=False))
+    cols = np.sort(rng.choice(N, ncols, replace=False))
+    ref = og.reference_rows_cols(aq, as_, bq, bs, FMTS[fmt], rows, cols)
+    err = og.gate_error(got[np.ix_(rows, cols)], ref)
+    assert err <= TOL, err
+
+
+def test_full_size_square_sampled(lib):
+    """8192 x 4096 activations times 4096 x 4096 weights (MXFP8 E4M3)."""
+    _sampled(lib, 8192, 4096, 4096, "e4m3", lambda m, k: inputs.activations(m, k, seed=0),
+             lambda n, k: inputs.weights(n, k, seed=4))
+
+
+def test_full_size_ffn_sampled(lib):
+    """8192 x 4096 activations times 14336 x 4096 weights (MXFP8 E4M3)."""
+    _sampled(lib, 8192, 14336, 4096, "e4m3", lambda m, k: inputs.activations(m, k, seed=0),
+             lambda n, k: inputs.weights(n, k, seed=5))
+
+
+def test_full_size_fp4_sampled(lib):
+    """4096 x 14336 gradient times 4096 x 14336 operand (MXFP4 E2M1)."""
+    _sampled(lib, 4096, 4096, 14336, "e2m1", lambda m, k: inputs.heavy_gradient(m, k, seed=6),
+             lambda n, k: inputs.fp4_operand(n, k, seed=8))
+
+
+def test_device_status_clean_after_gemm(lib):
+    assert lib.last_device_status() == 0

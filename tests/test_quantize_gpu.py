@@ -1,0 +1,290 @@
+"""GPU parity of the quantizers against the CPU oracle, bit for bit.
+
+Every code byte, scale byte, amax and ring slot produced by the CUDA library
+(called through its C ABI via the binding) must equal the oracle's on the
+same seeded bf16 inputs.  Sizes span several 128 x 128 tiles and ragged
+tails; full workload sizes are covered on sampled rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_02_gb300 import inputs
+from oracle import formats as F
+from oracle import mx as omx
+from oracle import pertensor as opt
+from tests.helpers import assert_bytes_equal, f64, np_
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2, "e2m1": F.E2M1}
+ORI = {"row": omx.ROW, "col": omx.COL, "dual": omx.DUAL}
+MODE = {"floor": omx.FLOOR, "ceil": omx.CEIL}
+
+
+def run_both(lib, x, fmt, orient, mode, rounding="rne", had=False, sr_key=0, had_seed=7, sf="canonical"):
+    dev = torch.device("cuda")
+    out = lib.mx_quantize(x.to(dev), fmt, orient, mode, rounding, had, sr_key, had_seed, sf)
+    ref = omx.quantize(f64(x), FMTS[fmt], ORI[orient], MODE[mode], omx.SR if rounding == "sr" else omx.RNE,
+                       had, sr_key, had_seed)
+    return [np_(t) for t in out], ref
+
+
+def check(got, ref, orient, sf="canonical", rows=None, cols=None):
+    qr, sr, qc, sc = got
+    if ORI[orient] & omx.ROW:
+        assert_bytes_equal(qr, ref["q_row"], "q_row")
+        s = ref["s_row"] if sf == "canonical" else omx.sf_to_mma(ref["s_row"])
+        assert_bytes_equal(sr.reshape(s.shape), s, "s_row")
+    if ORI[orient] & omx.COL:
+        assert_bytes_equal(qc, ref["q_col"], "q_col")
+        s = ref["s_col"] if sf == "canonical" else omx.sf_to_mma(ref["s_col"])
+        assert_bytes_equal(sc.reshape(s.shape), s, "s_col")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+@pytest.mark.parametrize("mode", ["floor", "ceil"])
+def test_mx_rne_tiles_and_ragged(lib, fmt, orient, mode):
+    # 288 x 416: three row tiles (the last one 32 rows), four column tiles (ragged)
+    x = inputs.small_rowwise(288, 416, seed=11)
+    got, ref = run_both(lib, x, fmt, orient, mode)
+    check(got, ref, orient)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+def test_mx_mma_scale_layout(lib, fmt, orient):
+    x = inputs.activations(256, 384, seed=3)
+    got, ref = run_both(lib, x, fmt, orient, "floor", sf="mma")
+    check(got, ref, orient, sf="mma")
+
+
+def test_small_rowwise_workload_and_dequant(lib):
+    """256 x 512 row-wise E4M3, floor scale, RNE, then dequantize (the small
+    row-wise workload), bf16 and float32 outputs."""
+    x = inputs.small_rowwise()
+    got, ref = run_both(lib, x, "e4m3", "row", "floor")
+    check(got, ref, "row")
+    dev = torch.device("cuda")
+    q, s = torch.from_numpy(ref["q_row"]).to(dev), torch.from_numpy(ref["s_row"]).to(dev)
+    want = omx.dequantize(ref["q_row"], ref["s_row"], F.E4M3)
+    d32 = lib.mx_dequantize(q, s, "e4m3", torch.float32)
+    assert_bytes_equal(np_(d32).view(np.uint32), want.astype(np.float32).view(np.uint32), "dequant f32")
+    d16 = lib.mx_dequantize(q, s, "e4m3", torch.bfloat16)
+    want16 = torch.from_numpy(want).to(torch.bfloat16).view(torch.int16).numpy()
+    assert_bytes_equal(np_(d16.view(torch.int16)), want16, "dequant bf16")
+    # the saturated +-1e4 entries decode to +-448 * X
+    assert np.sum(np.abs(want) == 448.0 * np.repeat(F.e8m0_decode(ref["s_row"]), 32, 1)) >= 4
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e2m1"])
+def test_dequant_other_formats(lib, fmt):
+    x = inputs.small_rowwise(96, 160, seed=5)
+    ref = omx.quantize(f64(x), FMTS[fmt], omx.ROW, omx.CEIL)
+    dev = torch.device("cuda")
+    d = lib.mx_dequantize(torch.from_numpy(ref["q_row"]).to(dev), torch.from_numpy(ref["s_row"]).to(dev), fmt)
+    want = omx.dequantize(ref["q_row"], ref["s_row"], FMTS[fmt]).astype(np.float32)
+    assert_bytes_equal(np_(d).view(np.uint32), want.view(np.uint32), "dequant")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+def test_special_values_and_edge_blocks(lib, fmt):
+    """Zero blocks (both signs), subnormal bf16, saturation, exact ties, NaN
+    and Inf blocks (scale 0xFF, zero codes)."""
+    sv = inputs.special_values_bf16()
+    rows = np.tile(sv, (128, 4)).astype(np.float32)         # 128 x 128
+    rng = np.random.default_rng(0)
+    rows *= np.exp2(rng.integers(-20, 20, size=(128, 1))).astype(np.float32)
+    rows[5, :32] = 0.0
+    rows[6, :32] = -0.0
+    rows[7, 40] = np.nan
+    rows[8, 70] = np.inf
+    rows[9, 100] = -np.inf
+    rows[64:96, 3] = np.nan                                  # a NaN column block
+    x = inputs.to_bf16(rows)
+    for orient in ("row", "col", "dual"):
+        for mode in ("floor", "ceil"):
+            got, ref = run_both(lib, x, fmt, orient, mode)
+            check(got, ref, orient)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+def test_all_rne_midpoints(lib, fmt):
+    """Every grid midpoint (a tie) and its neighbours, scaled so each block's
+    scale is 2^0: the kernel must pick the even code like the oracle."""
+    f = FMTS[fmt]
+    vals, _ = F._positive_grid(f)
+    mids = np.concatenate([(vals[:-1] + vals[1:]) / 2, vals, (vals[:-1] * 3 + vals[1:]) / 4])
+    mids = mids[np.abs(mids) < f.max_finite]
+    n = ((mids.size + 30) // 31) * 31
+    body = np.resize(mids, n).reshape(-1, 31)
+    blocks = np.concatenate([np.full((body.shape[0], 1), f.max_finite), body], axis=1)   # pin amax
+    blocks[::2] *= -1
+    x = np.resize(blocks.reshape(-1), 128 * 128).reshape(128, 128).astype(np.float32)
+    xb = inputs.to_bf16(x)
+    assert np.array_equal(f64(xb), x.astype(np.float64))     # all exact in bf16
+    got, ref = run_both(lib, xb, fmt, "row", "ceil")
+    check(got, ref, "row")
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e4m3"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+def test_stochastic_rounding_and_hadamard(lib, fmt, orient):
+    g = inputs.heavy_gradient(160, 288, seed=6)
+    for had in (False, True):
+        for key in (0, 0x123456789ABCDEF):
+            got, ref = run_both(lib, g, fmt, orient, "floor", "sr", had, key, 7)
+            check(got, ref, orient)
+
+
+@pytest.mark.parametrize("orient", ["row", "col"])
+def test_hadamard_rne(lib, orient):
+    x = inputs.activations(128, 256, seed=9)
+    got, ref = run_both(lib, x, "e2m1", orient, "ceil", "rne", True, 0, 7)
+    check(got, ref, orient)
+
+
+def test_dual_equals_single_orientations(lib):
+    """One read for both copies: the dual outputs are byte-identical to the
+    row-only and column-only runs."""
+    x = inputs.gradients(384, 256, seed=1)
+    dev = torch.device("cuda")
+    xd = x.to(dev)
+    for fmt in ("e4m3", "e5m2", "e2m1"):
+        d = lib.mx_quantize(xd, fmt, "dual", "ceil")
+        r = lib.mx_quantize(xd, fmt, "row", "ceil")
+        c = lib.mx_quantize(xd, fmt, "col", "ceil")
+        assert torch.equal(d[0], r[0]) and torch.equal(d[1], r[1])
+        assert torch.equal(d[2], c[2]) and torch.equal(d[3], c[3])
+
+
+def test_strided_input(lib):
+    base = inputs.activations(256, 512, seed=2)
+    x = base[:, 64:320]                              # row stride 512, 256 columns
+    dev = torch.device("cuda")
+    out = lib.mx_quantize(base.to(dev)[:, 64:320], "e4m3", "dual", "floor")
+    ref = omx.quantize(f64(x.contiguous()), F.E4M3, omx.DUAL, omx.FLOOR)
+    check([np_(t) for t in out], ref, "dual")
+
+
+def test_determinism(lib):
+    g = inputs.heavy_gradient(256, 256, seed=6).cuda()
+    a = lib.mx_quantize(g, "e2m1", "dual", "floor", "sr", True, 5, 7)
+    b = lib.mx_quantize(g, "e2m1", "dual", "floor", "sr", True, 5, 7)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+# ---------------------------------------------------------------- per-tensor FP8
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+def test_pertensor_no_ring(lib, fmt, orient):
+    x = inputs.small_rowwise(272, 400, seed=13)
+    dev = torch.device("cuda")
+    m = np.float32(0.37)
+    scale = torch.tensor([m], device=dev)
+    x8, x8T, amax = lib.fp8_quantize_pertensor(x.to(dev), scale, fmt, orient)
+    r8, r8T, ramax = opt.quantize_pertensor(f64(x), float(m), FMTS[fmt])
+    if orient in ("row", "dual"):
+        assert_bytes_equal(np_(x8), r8, "x8")
+    if orient in ("col", "dual"):
+        assert_bytes_equal(np_(x8T), r8T, "x8T")
+    assert float(amax.item()) == ramax
+
+
+def test_pertensor_ring_fold_sixteen_steps(lib):
+    """16 sequential steps with the in-kernel fold: every x8 / x8T byte and
+    every ring slot equals the oracle's host fold, exactly."""
+    dev = torch.device("cuda")
+    base = inputs.pertensor_base(512, 768, seed=2)
+    exps = inputs.pertensor_step_exponents(16, seed=3)
+    n = 16
+    ring = lib.ring_state_new(n, dev)
+    ring_ref = opt.ring_new(n)
+    for t, v in enumerate(exps):
+        xt = (base.float() * (2.0 ** v)).to(torch.bfloat16)
+        m = float(ring_ref[n + 1])
+        x8, x8T, amax = lib.quantize_dual(xt.to(dev), ring[n + 1:n + 2], "e4m3", ring, t % n, 448.0, 1.0)
+        r8, r8T, ramax = opt.quantize_pertensor(f64(xt), m, F.E4M3)
+        ring_ref = opt.ring_fold(ring_ref, ramax, t % n, 448.0, 1.0)
+        assert_bytes_equal(np_(x8), r8, f"x8 step {t}")
+        assert_bytes_equal(np_(x8T), r8T, f"x8T step {t}")
+        assert_bytes_equal(np_(ring).view(np.uint32), ring_ref.view(np.uint32), f"ring step {t}")
+        assert float(amax.item()) == 0.0          # the self-cleaned slot
+
+
+def test_pertensor_transposed_only_and_margin(lib):
+    dev = torch.device("cuda")
+    x = inputs.gradients(256, 384, seed=1)
+    ring = lib.ring_state_new(4, dev)
+    ring_ref = opt.ring_new(4)
+    for t in range(6):
+        xt = (x.float() * 2.0 ** (t % 3)).to(torch.bfloat16)
+        m = float(ring_ref[5])
+        x8T, _ = lib.quantize(xt.to(dev), ring[5:6], "e5m2", True, ring, t % 4, 57344.0, 2.0)
+        _, r8T, ramax = opt.quantize_pertensor(f64(xt), m, F.E5M2)
+        ring_ref = opt.ring_fold(ring_ref, ramax, t % 4, 57344.0, 2.0)
+        assert_bytes_equal(np_(x8T), r8T, "x8T")
+        assert_bytes_equal(np_(ring).view(np.uint32), ring_ref.view(np.uint32), "ring")
+
+
+# ---------------------------------------------------------------- full sizes (sampled)
+def _sample_rows(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, size=k, replace=False))
+
+
+@pytest.mark.parametrize("fmt,gen,seed", [("e4m3", inputs.activations, 0), ("e5m2", inputs.gradients, 1)])
+@pytest.mark.parametrize("mode", ["floor", "ceil"])
+def test_full_size_dual_sampled(lib, fmt, gen, seed, mode):
+    """8192 x 4096 dual quantize in the launch configuration the benchmark
+    times; rows (row copy) and 32-row slabs (column copy) sampled."""
+    x = gen(8192, 4096, seed=seed)
+    dev = torch.device("cuda")
+    qr, sr, qc, sc = lib.mx_quantize(x.to(dev), fmt, "dual", mode)
+    xv = f64(x)
+    rows = _sample_rows(8192, 96, 1)
+    ref = omx.quantize(xv[rows], FMTS[fmt], omx.ROW, MODE[mode])
+    assert_bytes_equal(np_(qr)[rows], ref["q_row"], "q_row sample")
+    assert_bytes_equal(np_(sr)[rows], ref["s_row"], "s_row sample")
+    slabs = _sample_rows(8192 // 32, 6, 2)
+    for sl in slabs:
+        r0 = sl * 32
+        refc = omx.quantize(xv[r0:r0 + 32], FMTS[fmt], omx.COL, MODE[mode])
+        assert_bytes_equal(np_(qc)[:, r0:r0 + 32], refc["q_col"], "q_col slab")
+        assert_bytes_equal(np_(sc)[:, sl:sl + 1], refc["s_col"], "s_col slab")
+
+
+def test_full_size_fp4_sr_hadamard_sampled(lib):
+    """4096 x 14336 MXFP4 with Hadamard-32 and stochastic rounding (key 0,
+    sign seed 7), sampled rows checked with their global element indices."""
+    g = inputs.heavy_gradient()
+    dev = torch.device("cuda")
+    q, s, _, _ = lib.mx_quantize(g.to(dev), "e2m1", "row", "floor", "sr", True, 0, 7, "mma")
+    gv = f64(g)
+    rows = _sample_rows(4096, 24, 3)
+    ref = omx.quantize(gv[rows], F.E2M1, omx.ROW, omx.FLOOR, omx.SR, True, 0, 7, row_index=rows, total_cols=14336)
+    assert_bytes_equal(np_(q)[rows], ref["q_row"], "q sample")
+    s_can = omx.sf_from_mma(np_(s), 4096, 14336 // 32)
+    assert_bytes_equal(s_can[rows], ref["s_row"], "s sample")
+
+
+def test_full_size_pertensor_one_step(lib):
+    dev = torch.device("cuda")
+    x = inputs.pertensor_base()
+    ring = lib.ring_state_new(16, dev)
+    x8, x8T, _ = lib.quantize_dual(x.to(dev), ring[17:18], "e4m3", ring, 0)
+    xv = f64(x)
+    rows = _sample_rows(4096, 32, 4)
+    r8, _, _ = opt.quantize_pertensor(xv[rows], 1.0, F.E4M3)
+    assert_bytes_equal(np_(x8)[rows], r8, "x8 sample")
+    assert torch.equal(x8T, x8.t().contiguous())
+    ramax = float(np.max(np.abs(xv)))
+    r = np_(ring)
+    assert r[0] == np.float32(ramax)
+    assert r[16] == np.float32(np.float64(np.float32(ramax)) / 448.0)
+
+
+def test_device_status_clean(lib):
+    assert lib.last_device_status() == 0
