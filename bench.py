@@ -122,12 +122,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# A GPU-side spin enqueued before each timed loop, long enough for the host
+# to queue every launch of the loop behind it: the event pairs then time the
+# kernels, not gaps while the GPU waits for Python to submit the next launch.
+HOST_LEAD_CYCLES = 60_000_000
+
+
 def make_timer(torch, flush):
     """Run fn() K times, each after an L2 flush, and return the mean device
     time (ms) of fn measured with CUDA events on the current stream."""
     def run(fn, k):
         st = torch.cuda.current_stream()
         evs = []
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         for _ in range(k):
             flush()
             a = torch.cuda.Event(enable_timing=True)
@@ -401,6 +408,7 @@ def run_ours(args, rank, world):
     per_launch = []
     st = torch.cuda.current_stream(dev)
     evs = []
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
     for _ in range(args.steps):
         for i in range(4):
             flush()

@@ -278,7 +278,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int q = warp & 3;                                      // tensor-memory lane quarter
     const int row = q * 32 + lane;                               // row within the tile
     const bool leader = (warp == EPI_WARP0 && lane == 0);
-    const int cw = p.out_fp32 ? 16 : 32;                         // columns per 64-byte chunk
     int t = 0, buf = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++t) {
       const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
@@ -287,6 +286,46 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
+      if (!p.out_fp32) {
+        // bf16: drain the whole accumulator row into registers first, so the
+        // MMA warp can start the next tile while this one is written out
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            pk[c * 16 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(acc_empty));
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          named_bar(1, 128);
+          uint8_t* stg = sOut + buf * STG_BYTES;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int phys = j ^ ((row >> 1) & 3);               // 64-byte swizzle
+            *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
+                make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          named_bar(1, 128);
+          if (leader) {
+            tma_store_2d(&map_c, smem_u32(stg), n0 + c * 32, m0);
+            bulk_commit();
+          }
+          buf ^= 1;
+        }
+        continue;
+      }
+      // float32 output: chunk by chunk
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
@@ -296,32 +335,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(acc_empty));
         }
-        const int nchunks = p.out_fp32 ? 2 : 1;
-        for (int h = 0; h < nchunks; ++h) {
-          uint32_t w[16];
-          if (p.out_fp32) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = v[h * 16 + j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-              w[j] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-          }
-          // the staging buffer we are about to fill must be drained
+        for (int h = 0; h < 2; ++h) {
           if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
           named_bar(1, 128);
           uint8_t* stg = sOut + buf * STG_BYTES;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int phys = j ^ ((row >> 1) & 3);               // 64-byte swizzle
-            *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
+                make_uint4(v[h * 16 + 4 * j], v[h * 16 + 4 * j + 1], v[h * 16 + 4 * j + 2], v[h * 16 + 4 * j + 3]);
           }
           fence_proxy_async_smem();
           named_bar(1, 128);
           if (leader) {
-            tma_store_2d(&map_c, smem_u32(stg), n0 + c0 + h * cw, m0);
+            tma_store_2d(&map_c, smem_u32(stg), n0 + c0 + h * 16, m0);
             bulk_commit();
           }
           buf ^= 1;

@@ -119,24 +119,11 @@ __device__ __forceinline__ uint32_t sr_draw(uint64_t idx, uint32_t k0, uint32_t 
 
 constexpr float kHadC = 0.17677669529663688f;  // float32 nearest 1/sqrt(32)
 
-// In-register butterfly stages h = 1, 2, 4 over 8 consecutive block
-// positions: (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h}).
-__device__ __forceinline__ void fwht8(float* u) {
-#pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if ((i & h) == 0) {
-        const float a = u[i], b = u[i + h];
-        u[i] = __fadd_rn(a, b);
-        u[i + h] = __fsub_rn(a, b);
-      }
-    }
-  }
-}
-
-// Full 32-point transform of a block held by one thread (column pass).
-__device__ __forceinline__ void hadamard32_local(float* u, uint32_t signs) {
+// Fixed-sign 32-point Hadamard of one block held by one thread:
+// u_j = s_j v_j; butterflies h = 1, 2, 4, 8, 16 in that order,
+// (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h}) for (i & h) == 0;
+// y_j = RN32(u_j * c).  Every operation is a separate float32 rounding.
+__device__ __forceinline__ void hadamard32(float (&u)[32], uint32_t signs) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) u[j] = ((signs >> j) & 1u) ? -u[j] : u[j];
 #pragma unroll
@@ -154,41 +141,63 @@ __device__ __forceinline__ void hadamard32_local(float* u, uint32_t signs) {
   for (int j = 0; j < 32; ++j) u[j] = __fmul_rn(u[j], kHadC);
 }
 
-// 32-point transform of a row block spread over 4 lanes (8 values each, block
-// position = 8 * (lane & 3) + j): stages 1, 2, 4 in registers, then 8 and 16
-// across lanes (xor 1, xor 2).
-__device__ __forceinline__ void hadamard32_row(float* u, int sub, uint32_t signs) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) u[j] = ((signs >> (sub * 8 + j)) & 1u) ? -u[j] : u[j];
-  fwht8(u);
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int bit = 1 << s;               // lane bit for h = 8 (s=0), 16 (s=1)
-    const bool upper = (sub & bit) != 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float other = __shfl_xor_sync(0xFFFFFFFFu, u[j], bit);
-      u[j] = upper ? __fsub_rn(other, u[j]) : __fadd_rn(u[j], other);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(u[j], kHadC);
-}
-
 __device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
-// Encode 8 scaled values; returns packed codes (FP8: 8 bytes, E2M1: 4 bytes in .x).
-template <int FMT>
-__device__ __forceinline__ uint2 encode8(const float* y) {
-  if constexpr (FMT == MXQ_E2M1) {
-    uint32_t w = 0;
+// Largest |value| of 32 bf16 held as 16 packed words, as float32 bits:
+// sign bits cleared, then 16-bit unsigned max (non-negative bf16 patterns
+// order like their values; NaN patterns sort above Inf).
+__device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t (&w)[16]) {
+  uint32_t m = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
-    return make_uint2(w, 0u);
+  for (int j = 0; j < 16; ++j) m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16) << 16;
+}
+
+// Quantize one 32-element block v (float32 values, exact) whose amax bits
+// are ab.  Codes go to out (FP8: 8 words, E2M1: 4 words, element 0 in the
+// lowest byte / nibble); returns the UE8M0 scale byte.  idx0 / istep give
+// the flat input index of element j as idx0 + j * istep (for the SR draw).
+template <int FMT, bool EXTRA>
+__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t ab, const QuantParams& p,
+                                                  uint64_t idx0, uint64_t istep, uint32_t (&out)[8]) {
+  const bool bad = ab >= 0x7F800000u;                 // NaN or Inf in the block
+  const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
+  const float m = exp2_neg(e);
+  float y[32];
+  if (EXTRA && p.rounding == MXQ_SR) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      y[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw(idx0 + j * istep, p.sr_k0, p.sr_k1));
   } else {
-    uint32_t w0 = cvt_fp8x2<FMT>(y[0], y[1]) | (cvt_fp8x2<FMT>(y[2], y[3]) << 16);
-    uint32_t w1 = cvt_fp8x2<FMT>(y[4], y[5]) | (cvt_fp8x2<FMT>(y[6], y[7]) << 16);
-    return make_uint2(w0, w1);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(v[j], m);
+  }
+  if constexpr (FMT == MXQ_E2M1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x |= cvt_e2m1x2(y[8 * k + 2 * j], y[8 * k + 2 * j + 1]) << (8 * j);
+      out[k] = bad ? 0u : x;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t x = cvt_fp8x2<FMT>(y[4 * k], y[4 * k + 1]) | (cvt_fp8x2<FMT>(y[4 * k + 2], y[4 * k + 3]) << 16);
+      out[k] = bad ? 0u : x;
+    }
+  }
+  return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+}
+
+// Per-tensor FP8 of 32 values: RNE-saturating encode of RN32(x * mult).
+template <int FMT>
+__device__ __forceinline__ void pertensor32(const uint32_t (&w)[16], float mult, uint32_t (&out)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t a = w[2 * k], b = w[2 * k + 1];
+    out[k] = cvt_fp8x2<FMT>(__fmul_rn(bf16lo(a), mult), __fmul_rn(bf16hi(a), mult)) |
+             (cvt_fp8x2<FMT>(__fmul_rn(bf16lo(b), mult), __fmul_rn(bf16hi(b), mult)) << 16);
   }
 }
 
@@ -206,7 +215,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
   constexpr bool FP4 = (FMT == MXQ_E2M1);
-  constexpr int QB = FP4 ? TILE / 2 : TILE;              // code bytes per tile row
+  constexpr int QB = FP4 ? TILE / 2 : TILE;              // code bytes per staged row
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,54 +271,56 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     const uint8_t* in = in_s + s * IN_STAGE_BYTES;
 
     // ------------------------------------------------------------ row pass
+    // One lane per 1x32 block: a warp takes 32 consecutive rows of one of the
+    // tile's four column blocks.  Shared loads are 16-byte and conflict-free
+    // (the TMA 128-byte swizzle puts the 8 rows of a phase in 8 banks groups).
     if constexpr (DO_ROW) {
-      const int lr = lane & 15, rs = lane >> 4;
-      const int hh = lr >> 3, ch = lr & 7, sub = lr & 3;
-#pragma unroll 2
-      for (int it = warp; it < TILE / 2; it += THREADS / 32) {
-        const int r = it * 2 + rs;
-        const uint4 raw = *reinterpret_cast<const uint4*>(in + hh * HALF_BYTES + r * 128 + ((ch ^ (r & 7)) << 4));
-        float v[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
-                      bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
-        uint2 codes;
+#pragma unroll 1
+      for (int task = warp; task < 16; task += THREADS / 32) {
+        const int b = task & 3;
+        const int r = (task >> 2) * 32 + lane;
+        const uint8_t* src = in + (b >> 1) * HALF_BYTES + r * 128;
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 q = *reinterpret_cast<const uint4*>(src + ((((b & 1) * 4 + k) ^ (r & 7)) << 4));
+          w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
+        }
+        uint32_t out[8];
         if constexpr (PERTENSOR) {
-          uint32_t ab = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) { ab = max(ab, absbits(v[j])); v[j] = __fmul_rn(v[j], mult); }
-          amax_acc = max(amax_acc, ab);
-          codes = encode8<FMT>(v);
+          amax_acc = max(amax_acc, amax_bf16x32(w));
+          pertensor32<FMT>(w, mult, out);
         } else {
-          if (EXTRA && p.hadamard) hadamard32_row(v, sub, signs);
-          uint32_t ab = 0;
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ab = max(ab, absbits(v[j]));
-          ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
-          ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
-          const bool bad = ab >= 0x7F800000u;
-          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
-          const float m = exp2_neg(e);
-          if (EXTRA && p.rounding == MXQ_SR) {
-            const uint64_t base = static_cast<uint64_t>(r0 + r) * static_cast<uint64_t>(p.cols) + (c0 + lr * 8);
+          for (int j = 0; j < 16; ++j) { v[2 * j] = bf16lo(w[j]); v[2 * j + 1] = bf16hi(w[j]); }
+          uint32_t ab;
+          if (EXTRA && p.hadamard) {
+            hadamard32(v, signs);
+            ab = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              v[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw(base + j, p.sr_k0, p.sr_k1));
+            for (int j = 0; j < 32; ++j) ab = max(ab, absbits(v[j]));
           } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], m);
+            ab = amax_bf16x32(w);
           }
-          codes = encode8<FMT>(v);
-          if (bad) codes = make_uint2(0u, 0u);
-          if (sub == 0) scr_s[sf_stage_off(r, lr >> 2, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+          const uint64_t idx0 = static_cast<uint64_t>(r0 + r) * static_cast<uint64_t>(p.cols) + (c0 + 32 * b);
+          const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, 1, out);
+          scr_s[sf_stage_off(r, b, p.sf_mma)] = static_cast<uint8_t>(sc);
         }
         if constexpr (FP4) {
-          *reinterpret_cast<uint32_t*>(qrow_s + r * QB + lr * 4) = codes.x;
+          // [128 rows][64 B], 64-byte swizzle: 16-B chunk index ^= (row >> 1) & 3
+          *reinterpret_cast<uint4*>(qrow_s + r * 64 + ((b ^ ((r >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
         } else {
-          *reinterpret_cast<uint2*>(qrow_s + r * QB + lr * 8) = codes;
+          // [128 rows][128 B], 128-byte swizzle: 16-B chunk index ^= row & 7
+          *reinterpret_cast<uint4*>(qrow_s + r * 128 + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(qrow_s + r * 128 + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
         }
       }
     }
 
     // ------------------------------------------------------------ column pass
+    // One lane per two adjacent columns x 32 rows (4-byte shared loads, a
+    // warp reads 128 contiguous bytes of a row: conflict-free).
     if constexpr (DO_COL) {
       const int hh = warp & 1, rb = warp >> 1;
       const int chk = lane >> 2, wb = (lane & 3) * 4;
@@ -319,65 +330,48 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
         const int row = rb * 32 + k;
         w[k] = *reinterpret_cast<const uint32_t*>(in + hh * HALF_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
       }
+      uint32_t m2 = 0;                       // packed amax of both columns
+      if (!EXTRA || !p.hadamard) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) m2 = __vmaxu2(m2, w[k] & 0x7FFF7FFFu);
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cl = hh * 64 + 2 * lane + half;       // tile column
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = half ? bf16hi(w[k]) : bf16lo(w[k]);
-        uint32_t cw[8];
+        uint32_t out[8];
         if constexpr (PERTENSOR) {
-          uint32_t ab = 0;
+          if (!DO_ROW) amax_acc = max(amax_acc, half ? (m2 & 0xFFFF0000u) : (m2 << 16));
 #pragma unroll
-          for (int k = 0; k < 32; ++k) { ab = max(ab, absbits(v[k])); v[k] = __fmul_rn(v[k], mult); }
-          if (!DO_ROW) amax_acc = max(amax_acc, ab);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) cw[k] = cvt_fp8x2<FMT>(v[4 * k], v[4 * k + 1]) | (cvt_fp8x2<FMT>(v[4 * k + 2], v[4 * k + 3]) << 16);
+          for (int k = 0; k < 8; ++k) {
+            const float a0 = __fmul_rn(half ? bf16hi(w[4 * k]) : bf16lo(w[4 * k]), mult);
+            const float a1 = __fmul_rn(half ? bf16hi(w[4 * k + 1]) : bf16lo(w[4 * k + 1]), mult);
+            const float a2 = __fmul_rn(half ? bf16hi(w[4 * k + 2]) : bf16lo(w[4 * k + 2]), mult);
+            const float a3 = __fmul_rn(half ? bf16hi(w[4 * k + 3]) : bf16lo(w[4 * k + 3]), mult);
+            out[k] = cvt_fp8x2<FMT>(a0, a1) | (cvt_fp8x2<FMT>(a2, a3) << 16);
+          }
         } else {
-          if (EXTRA && p.hadamard) hadamard32_local(v, signs);
-          uint32_t ab = 0;
+          float v[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
-          const bool bad = ab >= 0x7F800000u;
-          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
-          const float m = exp2_neg(e);
-          if (EXTRA && p.rounding == MXQ_SR) {
-            const int c = c0 + cl;
+          for (int k = 0; k < 32; ++k) v[k] = half ? bf16hi(w[k]) : bf16lo(w[k]);
+          uint32_t ab = half ? (m2 & 0xFFFF0000u) : (m2 << 16);
+          if (EXTRA && p.hadamard) {
+            hadamard32(v, signs);
+            ab = 0;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const uint64_t idx = static_cast<uint64_t>(r0 + rb * 32 + k) * static_cast<uint64_t>(p.cols) + c;
-              v[k] = sr_round<FMT>(__fmul_rn(v[k], m), sr_draw(idx, p.sr_k0, p.sr_k1));
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __fmul_rn(v[k], m);
+            for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
           }
-          if constexpr (FP4) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t x = 0;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) x |= cvt_e2m1x2(v[8 * k + 2 * j], v[8 * k + 2 * j + 1]) << (8 * j);
-              cw[k] = bad ? 0u : x;
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t x = cvt_fp8x2<FMT>(v[4 * k], v[4 * k + 1]) | (cvt_fp8x2<FMT>(v[4 * k + 2], v[4 * k + 3]) << 16);
-              cw[k] = bad ? 0u : x;
-            }
-          }
-          scc_s[sf_stage_off(cl, rb, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+          const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
+          const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
+          scc_s[sf_stage_off(cl, rb, p.sf_mma)] = static_cast<uint8_t>(sc);
         }
         if constexpr (FP4) {
-          // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (addr >> 7) & 3
-          const int phys = (rb ^ ((cl >> 1) & 3)) << 4;
-          *reinterpret_cast<uint4*>(qcol_s + cl * 64 + phys) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (col >> 1) & 3
+          *reinterpret_cast<uint4*>(qcol_s + cl * 64 + ((rb ^ ((cl >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
         } else {
           // [128 cols][128 B], 128-byte swizzle: 16-B chunk index ^= col & 7
           const int c7 = cl & 7;
-          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
         }
       }
     }
@@ -614,7 +608,7 @@ int make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, bool fp4, i
   if (orient & MXQ_ROW) {
     const uint64_t inner = fp4 ? cols / 2 : cols;
     if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qb, TILE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return MXQ_ERR_CUDA;
   }
   if (orient & MXQ_COL) {
