@@ -11,6 +11,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mxq.h"
 
 namespace mxq {
@@ -63,16 +65,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about hint_ns elapse, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and records a timeout) if it did not complete within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  // spin for the first few microseconds (fast wake-up on the critical path),
+  // then sleep in the barrier between checks (no issue slots burnt)
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
-      record_timeout(status);
-      return false;
+    if ((it & 63u) == 0u) {
+      const unsigned long long dt = globaltimer_ns() - t0;
+      if (dt > kWaitLimitNs) {
+        record_timeout(status);
+        return false;
+      }
+      if (dt > 4000u) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+      }
     }
   }
 }
@@ -120,6 +144,16 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
       : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels are launched with programmatic stream serialization: a kernel may
+// start while the previous one in the stream is finishing.  Every thread
+// runs grid_dep_wait() before its first global-memory access (it returns once
+// the previous grid has completed and its writes are visible; a no-op when
+// there is none), so ordering is as for a plain launch; only the prologue
+// overlaps.  grid_dep_launch() lets the next kernel begin its own prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- bf16 / fp8 bits
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -134,6 +168,91 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
   } else {
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   }
+  return r;
+}
+
+// Four float32 to four FP8 codes in one word (a lowest byte, d highest):
+// two paired conversions whose 16-bit results are joined without shifts.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x4(float a, float b, float c, float d) {
+  uint32_t r;
+  if constexpr (FMT == MXQ_E4M3) {
+    asm("{\n\t.reg .b16 t0, t1;\n\tcvt.rn.satfinite.e4m3x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t1, %4, %3;\n\tmov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+  } else {
+    asm("{\n\t.reg .b16 t0, t1;\n\tcvt.rn.satfinite.e5m2x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 t1, %4, %3;\n\tmov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+  }
+  return r;
+}
+
+// The multiplier m twice, as the 64-bit operand of a packed f32x2 multiply.
+__device__ __forceinline__ uint64_t f32x2_splat(float m) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(m));
+  return r;
+}
+
+// FP8 codes of lo(wa), hi(wa), lo(wb), hi(wb) -- four bf16 values (packed
+// two per word, element 2i in the low half) each multiplied by m (RN, with
+// one packed f32x2 multiply per pair) and converted RNE-saturating.  Code of
+// the first element in the lowest byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x4_rows(uint32_t wa, uint32_t wb, uint64_t mm) {
+  uint32_t r;
+  if constexpr (FMT == MXQ_E4M3) {
+    asm("{\n\t.reg .b32 a0, a1, b0, b1;\n\t.reg .b64 pa, pb;\n\t.reg .b16 t0, t1;\n\t"
+        "shl.b32 a0, %1, 16;\n\tand.b32 a1, %1, 0xFFFF0000;\n\t"
+        "shl.b32 b0, %2, 16;\n\tand.b32 b1, %2, 0xFFFF0000;\n\t"
+        "mov.b64 pa, {a0, a1};\n\tmov.b64 pb, {b0, b1};\n\t"
+        "mul.rn.f32x2 pa, pa, %3;\n\tmul.rn.f32x2 pb, pb, %3;\n\t"
+        "mov.b64 {a0, a1}, pa;\n\tmov.b64 {b0, b1}, pb;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t0, a1, a0;\n\tcvt.rn.satfinite.e4m3x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "r"(wa), "r"(wb), "l"(mm));
+  } else {
+    asm("{\n\t.reg .b32 a0, a1, b0, b1;\n\t.reg .b64 pa, pb;\n\t.reg .b16 t0, t1;\n\t"
+        "shl.b32 a0, %1, 16;\n\tand.b32 a1, %1, 0xFFFF0000;\n\t"
+        "shl.b32 b0, %2, 16;\n\tand.b32 b1, %2, 0xFFFF0000;\n\t"
+        "mov.b64 pa, {a0, a1};\n\tmov.b64 pb, {b0, b1};\n\t"
+        "mul.rn.f32x2 pa, pa, %3;\n\tmul.rn.f32x2 pb, pb, %3;\n\t"
+        "mov.b64 {a0, a1}, pa;\n\tmov.b64 {b0, b1}, pb;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 t0, a1, a0;\n\tcvt.rn.satfinite.e5m2x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "r"(wa), "r"(wb), "l"(mm));
+  }
+  return r;
+}
+
+// FP8 codes of one column of four consecutive rows: the low (HALF = 0) or
+// high (HALF = 1) bf16 of words w0..w3, multiplied by m and converted as in
+// fp8x4_rows.  Code of w0's element in the lowest byte.
+template <int FMT, int HALF>
+__device__ __forceinline__ uint32_t fp8x4_col(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint64_t mm) {
+  uint32_t r;
+#define MXQ_COL_BODY(EXTRACT, CVT)                                                         \
+  asm("{\n\t.reg .b32 a0, a1, b0, b1;\n\t.reg .b64 pa, pb;\n\t.reg .b16 t0, t1;\n\t" \
+      EXTRACT                                                                            \
+      "mov.b64 pa, {a0, a1};\n\tmov.b64 pb, {b0, b1};\n\t"                             \
+      "mul.rn.f32x2 pa, pa, %5;\n\tmul.rn.f32x2 pb, pb, %5;\n\t"                      \
+      "mov.b64 {a0, a1}, pa;\n\tmov.b64 {b0, b1}, pb;\n\t"                             \
+      CVT " t0, a1, a0;\n\t" CVT " t1, b1, b0;\n\t"                                    \
+      "mov.b32 %0, {t0, t1};\n\t}"                                                      \
+      : "=r"(r) : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(mm))
+#define MXQ_LO "shl.b32 a0, %1, 16;\n\tshl.b32 a1, %2, 16;\n\tshl.b32 b0, %3, 16;\n\tshl.b32 b1, %4, 16;\n\t"
+#define MXQ_HI "and.b32 a0, %1, 0xFFFF0000;\n\tand.b32 a1, %2, 0xFFFF0000;\n\tand.b32 b0, %3, 0xFFFF0000;\n\tand.b32 b1, %4, 0xFFFF0000;\n\t"
+  if constexpr (FMT == MXQ_E4M3) {
+    if constexpr (HALF == 0) MXQ_COL_BODY(MXQ_LO, "cvt.rn.satfinite.e4m3x2.f32");
+    else MXQ_COL_BODY(MXQ_HI, "cvt.rn.satfinite.e4m3x2.f32");
+  } else {
+    if constexpr (HALF == 0) MXQ_COL_BODY(MXQ_LO, "cvt.rn.satfinite.e5m2x2.f32");
+    else MXQ_COL_BODY(MXQ_HI, "cvt.rn.satfinite.e5m2x2.f32");
+  }
+#undef MXQ_LO
+#undef MXQ_HI
+#undef MXQ_COL_BODY
   return r;
 }
 
@@ -190,6 +309,22 @@ bool device_ok();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int launch_status();
+
+// Launch kernel with programmatic stream serialization (see grid_dep_wait).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? launch_status() : MXQ_ERR_CUDA;
+}
 
 // Device address of the status word of the current device.
 int* status_ptr();

@@ -190,6 +190,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();                 // before any global-memory access
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_sf = tmem + BN;                          // column offset of the scale area
 
@@ -224,6 +226,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Descriptors of stage 0, k-slice 0; every other (stage, slice) is a
+      // plain add on the 14-bit start-address field (addresses stay < 256 KB).
+      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 0, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
+      uint32_t idesc[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(C::AB_TYPE, BN, BM, C::FP4 ? (kk & 1) * 2 : kk);
       int u = 0, t = 0;
       for (int tile = blockIdx.x; tile < p.ntiles && !*abort_flag; tile += gridDim.x, ++t) {
         if (!mbar_wait(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
@@ -238,32 +249,22 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           // scale chunks -> tensor memory (each 512-B chunk: 32 lanes x 16 B, x4 lane groups)
 #pragma unroll
           for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_cp_sf(sfa_t + 4 * c, smem_desc(smem_u32(sSFA + s * C::SFA_BYTES + c * 512), 0, 128, 0));
+            tc_cp_sf(sfa_t + 4 * c, sfa_desc0 + ((s * C::SFA_BYTES + c * 512) >> 4));
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
 #pragma unroll
             for (int c = 0; c < C::SF_CHUNKS; ++c)
-              tc_cp_sf(sfb_t + 4 * (BN / 128) * c + 4 * h,
-                       smem_desc(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES + c * 512), 0, 128, 0));
-          const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
+              tc_cp_sf(sfb_t + 4 * (BN / 128) * c + 4 * h, sfb_desc0 + ((s * C::SFB_BYTES + h * C::SFA_BYTES + c * 512) >> 4));
+          const uint64_t ad = a_desc0 + ((s * C::A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + ((s * C::B_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // 32 bytes of K per MMA (32 FP8 or 64 FP4 elements)
-            const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-            uint32_t sfa, sfb, id;
-            if constexpr (C::FP4) {
-              // K = 64: two scales per row; chunk kk / 2, byte pair (kk % 2) * 2
-              sfa = sfa_t + 4 * (kk >> 1);
-              id = (kk & 1) * 2;
-              // B: the BN rows of chunk kk / 2 sit in BN / 32 consecutive columns
-              sfb = sfb_t + 4 * (BN / 128) * (kk >> 1);
-            } else {
-              sfa = sfa_t;
-              sfb = sfb_t;
-              id = kk;
-            }
-            tc_mma<C::FP4>(tmem, ad, bd, instr_desc(C::AB_TYPE, BN, BM, id), sfa, sfb, (kb | kk) != 0);
+            // 32 bytes of K per MMA (32 FP8 or 64 FP4 elements).  E2M1: K = 64
+            // consumes two scales per row, chunk kk / 2, byte pair (kk % 2) * 2;
+            // the BN rows of B's chunk sit in BN / 32 consecutive columns.
+            const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
+            const uint32_t sfb = C::FP4 ? sfb_t + 4 * (BN / 128) * (kk >> 1) : sfb_t;
+            tc_mma<C::FP4>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit(smem_u32(&empty[s]));                       // stage free when these MMAs finish
         }
@@ -415,8 +416,7 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
     attr_set[dev & 63] = true;
   }
   const int grid = std::min(p.ntiles, sm_count());
-  kern<<<grid, THREADS, Cf::SMEM, st>>>(ma, mb, mc, p);
-  return launch_status();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), Cf::SMEM, st, ma, mb, mc, p);
 }
 
 }  // namespace

@@ -34,7 +34,7 @@ namespace mxq {
 
 constexpr int TILE = 128;
 constexpr int NST = 2;                      // input stages per CTA
-constexpr int THREADS = 256;
+constexpr int THREADS = 512;                // 16 warps per CTA, 2 CTAs per SM
 constexpr int IN_STAGE_BYTES = TILE * TILE * 2;   // 32 KiB (two 16 KiB halves)
 constexpr int HALF_BYTES = IN_STAGE_BYTES / 2;
 
@@ -61,25 +61,15 @@ template <> struct FmtInfo<MXQ_E4M3> { static constexpr int Ed = 8;  static cons
 template <> struct FmtInfo<MXQ_E5M2> { static constexpr int Ed = 15; static constexpr uint32_t md = 0x600000u; static constexpr int mbits = 2; static constexpr int emin = -14; static constexpr float maxv = 57344.f; };
 template <> struct FmtInfo<MXQ_E2M1> { static constexpr int Ed = 2;  static constexpr uint32_t md = 0x400000u; static constexpr int mbits = 1; static constexpr int emin = 0;   static constexpr float maxv = 6.f; };
 
-// Shared exponent e from the block amax given as float32 bits (>= 0, finite,
+// Shared exponent e from the block amax given as float32 bits (>= 0, finite;
 // bf16 values are exact float32): floor rule e = E(amax) - E(destmax); ceil
-// rule adds 1 when amax's mantissa exceeds destmax's.  amax == 0 -> -127.
+// rule adds 1 when amax's mantissa field exceeds destmax's.  A zero or
+// subnormal amax has E <= -127, so with E(destmax) >= 2 the clamp to
+// [-127, 127] gives -127 -- the amax == 0 rule -- without special cases.
 template <int FMT>
 __device__ __forceinline__ int scale_exp(uint32_t ab, int ceil_mode) {
-  if (ab == 0u) return -127;
-  int E;
-  uint32_t man;
-  const uint32_t bexp = ab >> 23;
-  if (bexp == 0u) {                       // float32 subnormal
-    const int lz = __clz(ab);             // leading 1 at bit 31 - lz
-    E = (31 - lz) - 149;
-    man = (ab << (lz - 8)) & 0x7FFFFFu;
-  } else {
-    E = static_cast<int>(bexp) - 127;
-    man = ab & 0x7FFFFFu;
-  }
-  int e = E - FmtInfo<FMT>::Ed;
-  if (ceil_mode && man > FmtInfo<FMT>::md) e += 1;
+  int e = static_cast<int>(ab >> 23) - 127 - FmtInfo<FMT>::Ed;
+  if (ceil_mode && (ab & 0x7FFFFFu) > FmtInfo<FMT>::md) e += 1;
   return max(-127, min(127, e));
 }
 
@@ -143,14 +133,80 @@ __device__ __forceinline__ void hadamard32(float (&u)[32], uint32_t signs) {
 
 __device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
+// Packed bf16x2 running max of |w| (NaN-propagating): m = max(m, |w|) per
+// 16-bit half.  m holds non-negative patterns (or NaN), w raw bf16 pairs.
+__device__ __forceinline__ uint32_t hmax2_abs(uint32_t m, uint32_t w) {
+  const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&m),
+                                       __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // Largest |value| of 32 bf16 held as 16 packed words, as float32 bits:
 // sign bits cleared, then 16-bit unsigned max (non-negative bf16 patterns
 // order like their values; NaN patterns sort above Inf).
 __device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t (&w)[16]) {
   uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
+  for (int j = 0; j < 16; ++j) m = hmax2_abs(m, w[j]);
   return max(m & 0xFFFFu, m >> 16) << 16;
+}
+
+// RNE quantization of a 1x32 block given as 16 packed bf16 words (element
+// 2j in the low half of word j), scale exponent e.  out: FP8 8 words /
+// E2M1 4 words.
+template <int FMT>
+__device__ __forceinline__ void rne_words16(const uint32_t (&w)[16], float m, uint32_t (&out)[8]) {
+  if constexpr (FMT == MXQ_E2M1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t a = w[4 * k + j];
+        x |= cvt_e2m1x2(__fmul_rn(bf16lo(a), m), __fmul_rn(bf16hi(a), m)) << (8 * j);
+      }
+      out[k] = x;
+    }
+  } else {
+    const uint64_t mm = f32x2_splat(m);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = fp8x4_rows<FMT>(w[2 * k], w[2 * k + 1], mm);
+  }
+}
+
+// RNE quantization of one 32x1 column block held as the low (half = 0) or
+// high (half = 1) halves of 32 words (row k in word k).
+template <int FMT>
+__device__ __forceinline__ void rne_col32(const uint32_t (&w)[32], int half, float m, uint32_t (&out)[8]) {
+  auto x = [&](int k) { return __fmul_rn(half ? bf16hi(w[k]) : bf16lo(w[k]), m); };
+  if constexpr (FMT != MXQ_E2M1) {
+    const uint64_t mm = f32x2_splat(m);
+    if (half) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) out[k] = fp8x4_col<FMT, 1>(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3], mm);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) out[k] = fp8x4_col<FMT, 0>(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3], mm);
+    }
+    return;
+  }
+  if constexpr (FMT == MXQ_E2M1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v |= cvt_e2m1x2(x(8 * k + 2 * j), x(8 * k + 2 * j + 1)) << (8 * j);
+      out[k] = v;
+    }
+  }
+}
+
+// A block holding NaN or Inf gets zero codes (warp-uniform branch: rare).
+__device__ __forceinline__ void zero_if_bad(bool bad, uint32_t (&out)[8]) {
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = bad ? 0u : out[k];
+  }
 }
 
 // Quantize one 32-element block v (float32 values, exact) whose amax bits
@@ -183,7 +239,7 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
   } else {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t x = cvt_fp8x2<FMT>(y[4 * k], y[4 * k + 1]) | (cvt_fp8x2<FMT>(y[4 * k + 2], y[4 * k + 3]) << 16);
+      const uint32_t x = cvt_fp8x4<FMT>(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
       out[k] = bad ? 0u : x;
     }
   }
@@ -193,12 +249,9 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
 // Per-tensor FP8 of 32 values: RNE-saturating encode of RN32(x * mult).
 template <int FMT>
 __device__ __forceinline__ void pertensor32(const uint32_t (&w)[16], float mult, uint32_t (&out)[8]) {
+  const uint64_t mm = f32x2_splat(mult);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t a = w[2 * k], b = w[2 * k + 1];
-    out[k] = cvt_fp8x2<FMT>(__fmul_rn(bf16lo(a), mult), __fmul_rn(bf16hi(a), mult)) |
-             (cvt_fp8x2<FMT>(__fmul_rn(bf16lo(b), mult), __fmul_rn(bf16hi(b), mult)) << 16);
-  }
+  for (int k = 0; k < 8; ++k) out[k] = fp8x4_rows<FMT>(w[2 * k], w[2 * k + 1], mm);
 }
 
 // Offsets of the scale byte of (row r, block b) of a 128 x 4 staging chunk.
@@ -209,7 +262,7 @@ __device__ __forceinline__ int sf_stage_off(int r, int b, int mma) {
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, EXTRA ? 1 : 2)
 quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
                    const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
@@ -229,7 +282,6 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t signs = (EXTRA && p.hadamard) ? hadamard_sign_mask(p.had_k0, p.had_k1) : 0u;
-  const float mult = PERTENSOR ? *p.scale : 1.0f;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&bars[s]), 1);
@@ -239,6 +291,9 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     if (DO_COL) prefetch_tensormap(&map_qcol);
   }
   __syncthreads();
+  grid_dep_launch();
+  grid_dep_wait();                 // before any global-memory access
+  const float mult = PERTENSOR ? *p.scale : 1.0f;
 
   int issued = 0;
   auto issue = [&](int i) {  // thread 0 only
@@ -264,19 +319,43 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     if (tile >= p.ntiles) break;
     const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
     const int s = i % NST;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), (i / NST) & 1, p.status);
+    const uint32_t full_bar = smem_u32(&bars[s]);
+    const uint32_t parity = (i / NST) & 1;
+    // Thread 0 alone waits for the tile's TMA loads (bounded) and for the
+    // previous tile's bulk stores to have left the staging buffers; the rest
+    // of the CTA waits at the barrier instead of spinning.
+    bool ok = true;
+    if (tid == 0) {
+      ok = mbar_wait(full_bar, parity, p.status);
+      bulk_wait_read_all();
+    }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
-    if (tid == 0) bulk_wait_read_all();     // staging buffers free again
-    __syncthreads();
+    // each thread observes the completed phase itself (acquire); it has
+    // completed, so this returns at once
+    if (!mbar_try_wait(full_bar, parity)) (void)mbar_wait(full_bar, parity, p.status);
     const uint8_t* in = in_s + s * IN_STAGE_BYTES;
 
+    // Work split: 16 row tasks (32 rows x one 32-column block, one lane per
+    // 1x32 block) and 8 column tasks (64 columns x 32 rows, one lane per two
+    // 32x1 blocks).  Dual: warps 0-7 take the row tasks, warps 8-15 the
+    // column tasks, so both passes run side by side.
+    int row_task0 = -1, row_task1 = -1, col_task = -1;
+    if constexpr (DO_ROW && DO_COL) {
+      if (warp < 8) { row_task0 = warp; row_task1 = warp + 8; } else { col_task = warp - 8; }
+    } else if constexpr (DO_ROW) {
+      row_task0 = warp;
+    } else {
+      if (warp < 8) col_task = warp;
+    }
+
     // ------------------------------------------------------------ row pass
-    // One lane per 1x32 block: a warp takes 32 consecutive rows of one of the
-    // tile's four column blocks.  Shared loads are 16-byte and conflict-free
-    // (the TMA 128-byte swizzle puts the 8 rows of a phase in 8 banks groups).
+    // Shared loads are 16-byte and conflict-free: the TMA 128-byte swizzle
+    // puts the 8 rows of a load phase in 8 different bank groups.
     if constexpr (DO_ROW) {
 #pragma unroll 1
-      for (int task = warp; task < 16; task += THREADS / 32) {
+      for (int t = 0; t < 2; ++t) {
+        const int task = t ? row_task1 : row_task0;
+        if (task < 0) break;
         const int b = task & 3;
         const int r = (task >> 2) * 32 + lane;
         const uint8_t* src = in + (b >> 1) * HALF_BYTES + r * 128;
@@ -290,12 +369,19 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
         if constexpr (PERTENSOR) {
           amax_acc = max(amax_acc, amax_bf16x32(w));
           pertensor32<FMT>(w, mult, out);
+        } else if constexpr (!EXTRA) {
+          const uint32_t ab = amax_bf16x32(w);
+          const bool bad = ab >= 0x7F800000u;
+          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
+          rne_words16<FMT>(w, exp2_neg(e), out);
+          zero_if_bad(bad, out);
+          scr_s[sf_stage_off(r, b, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
         } else {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) { v[2 * j] = bf16lo(w[j]); v[2 * j + 1] = bf16hi(w[j]); }
           uint32_t ab;
-          if (EXTRA && p.hadamard) {
+          if (p.hadamard) {
             hadamard32(v, signs);
             ab = 0;
 #pragma unroll
@@ -319,59 +405,58 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     }
 
     // ------------------------------------------------------------ column pass
-    // One lane per two adjacent columns x 32 rows (4-byte shared loads, a
-    // warp reads 128 contiguous bytes of a row: conflict-free).
+    // 4-byte shared loads: a warp reads 128 contiguous bytes of a row.
     if constexpr (DO_COL) {
-      const int hh = warp & 1, rb = warp >> 1;
-      const int chk = lane >> 2, wb = (lane & 3) * 4;
-      uint32_t w[32];
+      if (col_task >= 0) {
+        const int hh = col_task & 1, rb = col_task >> 1;
+        const int chk = lane >> 2, wb = (lane & 3) * 4;
+        uint32_t w[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int row = rb * 32 + k;
-        w[k] = *reinterpret_cast<const uint32_t*>(in + hh * HALF_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
-      }
-      uint32_t m2 = 0;                       // packed amax of both columns
-      if (!EXTRA || !p.hadamard) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) m2 = __vmaxu2(m2, w[k] & 0x7FFF7FFFu);
-      }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int cl = hh * 64 + 2 * lane + half;       // tile column
-        uint32_t out[8];
-        if constexpr (PERTENSOR) {
-          if (!DO_ROW) amax_acc = max(amax_acc, half ? (m2 & 0xFFFF0000u) : (m2 << 16));
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float a0 = __fmul_rn(half ? bf16hi(w[4 * k]) : bf16lo(w[4 * k]), mult);
-            const float a1 = __fmul_rn(half ? bf16hi(w[4 * k + 1]) : bf16lo(w[4 * k + 1]), mult);
-            const float a2 = __fmul_rn(half ? bf16hi(w[4 * k + 2]) : bf16lo(w[4 * k + 2]), mult);
-            const float a3 = __fmul_rn(half ? bf16hi(w[4 * k + 3]) : bf16lo(w[4 * k + 3]), mult);
-            out[k] = cvt_fp8x2<FMT>(a0, a1) | (cvt_fp8x2<FMT>(a2, a3) << 16);
-          }
-        } else {
-          float v[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = half ? bf16hi(w[k]) : bf16lo(w[k]);
-          uint32_t ab = half ? (m2 & 0xFFFF0000u) : (m2 << 16);
-          if (EXTRA && p.hadamard) {
-            hadamard32(v, signs);
-            ab = 0;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
-          }
-          const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
-          const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
-          scc_s[sf_stage_off(cl, rb, p.sf_mma)] = static_cast<uint8_t>(sc);
+        for (int k = 0; k < 32; ++k) {
+          const int row = rb * 32 + k;
+          w[k] = *reinterpret_cast<const uint32_t*>(in + hh * HALF_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
         }
-        if constexpr (FP4) {
-          // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (col >> 1) & 3
-          *reinterpret_cast<uint4*>(qcol_s + cl * 64 + ((rb ^ ((cl >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-        } else {
-          // [128 cols][128 B], 128-byte swizzle: 16-B chunk index ^= col & 7
-          const int c7 = cl & 7;
-          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-          *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+        uint32_t m2 = 0;                       // packed amax of both columns
+#pragma unroll
+        for (int k = 0; k < 32; ++k) m2 = hmax2_abs(m2, w[k]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int cl = hh * 64 + 2 * lane + half;       // tile column
+          uint32_t out[8];
+          const uint32_t abw = half ? (m2 & 0xFFFF0000u) : (m2 << 16);
+          if constexpr (PERTENSOR) {
+            if (!DO_ROW) amax_acc = max(amax_acc, abw);
+            rne_col32<FMT>(w, half, mult, out);
+          } else if constexpr (!EXTRA) {
+            const bool bad = abw >= 0x7F800000u;
+            const int e = scale_exp<FMT>(bad ? 0u : abw, p.ceil_mode);
+            rne_col32<FMT>(w, half, exp2_neg(e), out);
+            zero_if_bad(bad, out);
+            scc_s[sf_stage_off(cl, rb, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+          } else {
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = half ? bf16hi(w[k]) : bf16lo(w[k]);
+            uint32_t ab = abw;
+            if (p.hadamard) {
+              hadamard32(v, signs);
+              ab = 0;
+#pragma unroll
+              for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
+            }
+            const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
+            const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
+            scc_s[sf_stage_off(cl, rb, p.sf_mma)] = static_cast<uint8_t>(sc);
+          }
+          if constexpr (FP4) {
+            // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (col >> 1) & 3
+            *reinterpret_cast<uint4*>(qcol_s + cl * 64 + ((rb ^ ((cl >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          } else {
+            // [128 cols][128 B], 128-byte swizzle: 16-B chunk index ^= col & 7
+            const int c7 = cl & 7;
+            *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+          }
         }
       }
     }
@@ -562,7 +647,8 @@ template <int FMT, int ORIENT, bool PT, bool EXTRA>
 int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
                  cudaStream_t st) {
   auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA>;
-  const int smem = NST * IN_STAGE_BYTES + 16384 * 2 + 512 * 2 + 64 + 1024;
+  // stages, two staging tiles, two scale chunks, barriers + reduction (256 B), alignment slack
+  const int smem = NST * IN_STAGE_BYTES + 16384 * 2 + 512 * 2 + 256 + 1024;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -571,9 +657,8 @@ int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap
       return MXQ_ERR_CUDA;
     attr_set[dev & 63] = true;
   }
-  const int grid = std::min(p.ntiles, 2 * sm_count());
-  kern<<<grid, THREADS, smem, st>>>(mx, mr, mc, p);
-  return launch_status();
+  const int grid = std::min(p.ntiles, (EXTRA ? 1 : 2) * sm_count());
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), smem, st, mx, mr, mc, p);
 }
 
 template <bool PT>
