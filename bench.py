@@ -71,6 +71,25 @@ def gemm_flops(M, N, K):
     return 2 * M * N * K
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's step time (the job finishes when the last rank does)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_step_max: float) -> float:
+    """Whole-job GB/s: every rank quantizes its own same-size shard (no
+    data-path collective), so the job moves world x the per-rank bytes in
+    the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_step_max * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- timing helpers
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while the
@@ -441,12 +460,9 @@ def run_ours(args, rank, world):
     per_launch = [t / 4 for t in per_step]
     # for reference: one launch alone after an L2 flush (write + read-back)
     iso_ms = timed(lambda: launch_quant(0), 20)
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, dev)
     step_bytes = 4 * mx_quant_bytes(M, K)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = weak_scaling_value(step_bytes, world, ms_step)
     launch_ms = statistics.mean(per_launch)
     ach = mx_quant_bytes(M, K) / (launch_ms * 1e-3) / 1e9
 

@@ -63,8 +63,9 @@ def load() -> ctypes.CDLL:
     L.mxq_strerror.argtypes = [i32]
     L.mxq_strerror.restype = ctypes.c_char_p
     L.mxq_version.argtypes = []
+    L.mxq_test_stall_next_launch.argtypes = [i32]
     for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_sf_to_mma",
-                 "mxq_last_device_status", "mxq_version"):
+                 "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32
     _lib = L
     return L

@@ -12,9 +12,9 @@ __device__ int g_status = 0;
 
 namespace mxq_host {
 
+std::mutex g_mu;
 namespace {
 constexpr int kMaxDev = 64;
-std::mutex g_mu;
 int g_sms[kMaxDev] = {};
 int g_ok[kMaxDev] = {};          // 0 unknown, 1 ok, -1 not sm_103
 int* g_status_ptr[kMaxDev] = {};
@@ -90,6 +90,15 @@ int* status_ptr() {
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA; }
 
+int g_test_stall = 0;
+
+bool take_test_stall(int which) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_test_stall != which) return false;
+  g_test_stall = 0;
+  return true;
+}
+
 }  // namespace mxq_host
 
 extern "C" int mxq_last_device_status(void* stream) {
@@ -114,6 +123,13 @@ extern "C" const char* mxq_strerror(int s) {
     case MXQ_ERR_TIMEOUT: return "a bounded device wait expired";
     default: return "unknown status";
   }
+}
+
+extern "C" int mxq_test_stall_next_launch(int which) {
+  if (which != 0 && which != 1 && which != 2) return MXQ_ERR_BAD_ARG;
+  std::lock_guard<std::mutex> lk(mxq_host::g_mu);
+  mxq_host::g_test_stall = which;
+  return MXQ_OK;
 }
 
 extern "C" int mxq_version(void) { return 100; }

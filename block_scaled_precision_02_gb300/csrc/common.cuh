@@ -329,4 +329,8 @@ int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaS
 // Device address of the status word of the current device.
 int* status_ptr();
 
+// Failure-detection test hook: true (once) if mxq_test_stall_next_launch(which)
+// armed it (which: 1 quantizer, 2 GEMM).
+bool take_test_stall(int which);
+
 }  // namespace mxq_host

@@ -47,6 +47,7 @@ struct Params {
   int kb4;            // 512-byte scale chunks per 128 rows (K / 128)
   int out_fp32;
   int* status;
+  int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
 
 // ---------------------------------------------------------------- tcgen05 wrappers
@@ -205,6 +206,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
           const int s = u % STAGES;
           if (!mbar_wait(smem_u32(&empty[s]), ((u / STAGES) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
+          if (blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, C::TX_BYTES);
           tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, m0);
@@ -405,6 +407,7 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
   p.kb4 = static_cast<int>(K / 128);
   p.out_fp32 = out_fp32;
   p.status = status_ptr();
+  p.stall_u = take_test_stall(2) ? 0 : -1;
   if (!p.status) return MXQ_ERR_CUDA;
   auto kern = mx_gemm_kernel<FMT, BN>;
   static bool attr_set[64] = {};

@@ -52,6 +52,7 @@ struct QuantParams {
   int hist_len, hist_idx;
   float fp8_max, margin;
   float* amax_out;
+  int stall_tile;     // failure-detection test hook: this tile is never loaded (-1: off)
 };
 
 // destmax = m_d * 2^E_d: exponent and 23-bit mantissa field of the largest
@@ -133,21 +134,25 @@ __device__ __forceinline__ void hadamard32(float (&u)[32], uint32_t signs) {
 
 __device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
-// Packed bf16x2 running max of |w| (NaN-propagating): m = max(m, |w|) per
-// 16-bit half.  m holds non-negative patterns (or NaN), w raw bf16 pairs.
+// Packed bf16x2 running max of magnitudes, NaN-propagating, one instruction
+// per word: each half becomes max(|m|, |w|) with the XOR of the two signs;
+// callers clear the sign bits once at the end (amax_halves).
 __device__ __forceinline__ uint32_t hmax2_abs(uint32_t m, uint32_t w) {
-  const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&m),
-                                       __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w)));
-  return *reinterpret_cast<const uint32_t*>(&r);
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w));
+  return r;
 }
 
-// Largest |value| of 32 bf16 held as 16 packed words, as float32 bits:
-// sign bits cleared, then 16-bit unsigned max (non-negative bf16 patterns
-// order like their values; NaN patterns sort above Inf).
+// Sign-cleared halves of a hmax2_abs accumulator (NaN stays above Inf).
+__device__ __forceinline__ uint32_t amax_halves(uint32_t m) { return m & 0x7FFF7FFFu; }
+
+// Largest |value| of 32 bf16 held as 16 packed words, as float32 bits
+// (non-negative bf16 patterns order like their values; NaN sorts above Inf).
 __device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t (&w)[16]) {
   uint32_t m = 0;
 #pragma unroll
   for (int j = 0; j < 16; ++j) m = hmax2_abs(m, w[j]);
+  m = amax_halves(m);
   return max(m & 0xFFFFu, m >> 16) << 16;
 }
 
@@ -298,6 +303,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   int issued = 0;
   auto issue = [&](int i) {  // thread 0 only
     const int tile = blockIdx.x + i * gridDim.x;
+    if (tile == p.stall_tile) return;      // test hook: leave this stage's phase incomplete
     const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
     const uint32_t bar = smem_u32(&bars[i % NST]);
     uint8_t* dst = in_s + (i % NST) * IN_STAGE_BYTES;
@@ -419,6 +425,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
         uint32_t m2 = 0;                       // packed amax of both columns
 #pragma unroll
         for (int k = 0; k < 32; ++k) m2 = hmax2_abs(m2, w[k]);
+        m2 = amax_halves(m2);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int cl = hh * 64 + 2 * lane + half;       // tile column
@@ -746,6 +753,7 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   p.s_row = s_row;
   p.s_col = s_col;
   p.status = status_ptr();
+  p.stall_tile = take_test_stall(1) ? 0 : -1;
   if (!p.status) return MXQ_ERR_CUDA;
   return dispatch<false>(fmt, orient, mx, mr, mc, p, static_cast<cudaStream_t>(stream));
 }
@@ -784,6 +792,7 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
   p.fp8_max = fp8_max;
   p.margin = pow2_margin;
   p.amax_out = amax_out;
+  p.stall_tile = -1;
   if (!ring_state) {
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MXQ_ERR_CUDA;
   }

@@ -181,6 +181,17 @@ const char* mxq_strerror(int status);
 /* Library version, major*10000 + minor*100 + patch. */
 int mxq_version(void);
 
+/* Failure-detection test hook (no counterpart on the pages).  which = 1 arms
+ * the next mxq_quantize call, 2 the next mxq_gemm call, 0 disarms: in that
+ * launch CTA 0 leaves one of its input stages unloaded, so the mbarrier phase
+ * that stage's consumer waits on never completes.  The bounded wait expires
+ * after about a second, the kernel records MXQ_ERR_TIMEOUT in the device
+ * status word, winds all of its roles down (awaiting its own copies, with a
+ * limit, and releasing tensor memory) and exits; the CUDA context stays
+ * usable.  The launch's outputs are then unspecified.  Returns MXQ_OK, or
+ * MXQ_ERR_BAD_ARG for another value of which.  Not for production use. */
+int mxq_test_stall_next_launch(int which);
+
 #ifdef __cplusplus
 }
 #endif
