@@ -22,6 +22,8 @@ SOURCES = ["api.cu", "quantize.cu", "gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
                 "--expt-relaxed-constexpr", "-diag-suppress", "177"]
+# extra nvcc flags, e.g. the quantizer tile knobs -DMXQ_QUANT_TC=64 -DMXQ_QUANT_NST=3
+FLAGS += os.environ.get("MXQ_NVCC_FLAGS", "").split()
 
 
 def nvcc() -> str:

@@ -32,11 +32,36 @@
 
 namespace mxq {
 
-constexpr int TILE = 128;
-constexpr int NST = 2;                      // input stages per CTA
-constexpr int THREADS = 512;                // 16 warps per CTA, 2 CTAs per SM
-constexpr int IN_STAGE_BYTES = TILE * TILE * 2;   // 32 KiB (two 16 KiB halves)
-constexpr int HALF_BYTES = IN_STAGE_BYTES / 2;
+// Tile shape of the quantizers: 128 rows x TC columns of bf16, NSTG input
+// stages per CTA (build-time knobs; the defaults are the measured best).
+#ifndef MXQ_QUANT_TC
+#define MXQ_QUANT_TC 64
+#endif
+#ifndef MXQ_QUANT_NST
+#define MXQ_QUANT_NST 3
+#endif
+constexpr int TR = 128;                     // tile rows
+constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
+
+template <int TC, int NSTG, bool EXTRA>
+struct TileCfg {
+  static_assert(TC == 64 || TC == 128, "tile width");
+  static constexpr int THREADS = TC * 4;            // one warp per 8 tile columns
+  static constexpr int NW = THREADS / 32;
+  static constexpr int IN_BYTES = TR * TC * 2;
+  static constexpr int ROW_BLOCKS = TC / 32;        // 1x32 blocks per tile row
+  static constexpr int ROW_TASKS = 4 * ROW_BLOCKS;  // 32 rows x one block each (= NW)
+  static constexpr int COL_TASKS = TC / 16;         // 64 columns x 32 rows each (= NW / 2)
+  // resident CTAs per SM the registers are budgeted for
+  static constexpr int MIN_BLOCKS = EXTRA ? (TC == 128 ? 1 : 2)
+                                          : (TC == 128 ? 2 : (NSTG == 2 ? 4 : (NSTG == 3 ? 3 : 2)));
+};
+
+// 16-byte chunk index after the TMA swizzle of a staged row of `pitch`
+// bytes (128 / 64 / 32-byte swizzle: chunk bits ^= address bits 7..9 / 7..8 / 7).
+__device__ __forceinline__ int swz(int row, int chunk, int pitch) {
+  return chunk ^ (((row * pitch) >> 7) & (pitch / 16 - 1));
+}
 
 struct QuantParams {
   int rows, cols;
@@ -259,37 +284,36 @@ __device__ __forceinline__ void pertensor32(const uint32_t (&w)[16], float mult,
   for (int k = 0; k < 8; ++k) out[k] = fp8x4_rows<FMT>(w[2 * k], w[2 * k + 1], mm);
 }
 
-// Offsets of the scale byte of (row r, block b) of a 128 x 4 staging chunk.
-__device__ __forceinline__ int sf_stage_off(int r, int b, int mma) {
-  return mma ? ((r & 31) * 16 + ((r >> 5) & 3) * 4 + b) : (r * 4 + b);
-}
-
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
-template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA>
-__global__ void __launch_bounds__(THREADS, EXTRA ? 1 : 2)
+template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int TC, int NSTG>
+__global__ void __launch_bounds__(TileCfg<TC, NSTG, EXTRA>::THREADS, TileCfg<TC, NSTG, EXTRA>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
                    const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
+  using T = TileCfg<TC, NSTG, EXTRA>;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
   constexpr bool FP4 = (FMT == MXQ_E2M1);
-  constexpr int QB = FP4 ? TILE / 2 : TILE;              // code bytes per staged row
+  constexpr int QBR = FP4 ? TC / 2 : TC;            // code bytes per staged tile row
+  constexpr int QBC = FP4 ? TR / 2 : TR;            // code bytes per staged tile column
+  constexpr int ROWSTG = (TR * QBR + 1023) & ~1023;
+  constexpr int COLSTG = (TC * QBC + 1023) & ~1023;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* in_s = smem;
-  uint8_t* qrow_s = in_s + NST * IN_STAGE_BYTES;
-  uint8_t* qcol_s = qrow_s + 16384;
-  uint8_t* scr_s = qcol_s + 16384;
-  uint8_t* scc_s = scr_s + 512;
+  uint8_t* qrow_s = in_s + NSTG * T::IN_BYTES;
+  uint8_t* qcol_s = qrow_s + ROWSTG;
+  uint8_t* scr_s = qcol_s + COLSTG;      // [128 rows][ROW_BLOCKS] scale bytes
+  uint8_t* scc_s = scr_s + 512;          // [TC columns][4] scale bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(scc_s + 512);
-  uint32_t* red = reinterpret_cast<uint32_t*>(bars + NST);
+  uint32_t* red = reinterpret_cast<uint32_t*>(bars + NSTG);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t signs = (EXTRA && p.hadamard) ? hadamard_sign_mask(p.had_k0, p.had_k1) : 0u;
 
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < NSTG; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
     prefetch_tensormap(&map_x);
     if (DO_ROW) prefetch_tensormap(&map_qrow);
@@ -304,17 +328,30 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   auto issue = [&](int i) {  // thread 0 only
     const int tile = blockIdx.x + i * gridDim.x;
     if (tile == p.stall_tile) return;      // test hook: leave this stage's phase incomplete
-    const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
-    const uint32_t bar = smem_u32(&bars[i % NST]);
-    uint8_t* dst = in_s + (i % NST) * IN_STAGE_BYTES;
-    mbar_arrive_expect_tx(bar, IN_STAGE_BYTES);
-    tma_load_2d(smem_u32(dst), &map_x, bar, c0, r0);
-    tma_load_2d(smem_u32(dst + HALF_BYTES), &map_x, bar, c0 + 64, r0);
+    const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
+    const uint32_t bar = smem_u32(&bars[i % NSTG]);
+    uint8_t* dst = in_s + (i % NSTG) * T::IN_BYTES;
+    mbar_arrive_expect_tx(bar, T::IN_BYTES);
+#pragma unroll
+    for (int h = 0; h < TC / 64; ++h) tma_load_2d(smem_u32(dst + h * BOX_BYTES), &map_x, bar, c0 + 64 * h, r0);
   };
   if (tid == 0) {
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < NSTG; ++i) {
       if (blockIdx.x + i * gridDim.x < p.ntiles) { issue(i); issued = i + 1; }
     }
+  }
+
+  // Work split: row tasks (32 rows x one 32-column block, one lane per 1x32
+  // block) and column tasks (64 columns x 32 rows, one lane per two 32x1
+  // blocks).  Dual: the first half of the warps take two row tasks each,
+  // the second half one column task each, so both passes run side by side.
+  int row_task0 = -1, row_task1 = -1, col_task = -1;
+  if constexpr (DO_ROW && DO_COL) {
+    if (warp < T::NW / 2) { row_task0 = warp; row_task1 = warp + T::NW / 2; } else { col_task = warp - T::NW / 2; }
+  } else if constexpr (DO_ROW) {
+    row_task0 = warp;
+  } else {
+    if (warp < T::COL_TASKS) col_task = warp;
   }
 
   uint32_t amax_acc = 0;   // per-tensor: running max of |x| bits
@@ -323,10 +360,10 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   for (;; ++i) {
     const int tile = blockIdx.x + i * gridDim.x;
     if (tile >= p.ntiles) break;
-    const int r0 = (tile / p.tiles_c) * TILE, c0 = (tile % p.tiles_c) * TILE;
-    const int s = i % NST;
+    const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
+    const int s = i % NSTG;
     const uint32_t full_bar = smem_u32(&bars[s]);
-    const uint32_t parity = (i / NST) & 1;
+    const uint32_t parity = (i / NSTG) & 1;
     // Thread 0 alone waits for the tile's TMA loads (bounded) and for the
     // previous tile's bulk stores to have left the staging buffers; the rest
     // of the CTA waits at the barrier instead of spinning.
@@ -339,20 +376,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     // each thread observes the completed phase itself (acquire); it has
     // completed, so this returns at once
     if (!mbar_try_wait(full_bar, parity)) (void)mbar_wait(full_bar, parity, p.status);
-    const uint8_t* in = in_s + s * IN_STAGE_BYTES;
-
-    // Work split: 16 row tasks (32 rows x one 32-column block, one lane per
-    // 1x32 block) and 8 column tasks (64 columns x 32 rows, one lane per two
-    // 32x1 blocks).  Dual: warps 0-7 take the row tasks, warps 8-15 the
-    // column tasks, so both passes run side by side.
-    int row_task0 = -1, row_task1 = -1, col_task = -1;
-    if constexpr (DO_ROW && DO_COL) {
-      if (warp < 8) { row_task0 = warp; row_task1 = warp + 8; } else { col_task = warp - 8; }
-    } else if constexpr (DO_ROW) {
-      row_task0 = warp;
-    } else {
-      if (warp < 8) col_task = warp;
-    }
+    const uint8_t* in = in_s + s * T::IN_BYTES;
 
     // ------------------------------------------------------------ row pass
     // Shared loads are 16-byte and conflict-free: the TMA 128-byte swizzle
@@ -362,9 +386,9 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       for (int t = 0; t < 2; ++t) {
         const int task = t ? row_task1 : row_task0;
         if (task < 0) break;
-        const int b = task & 3;
-        const int r = (task >> 2) * 32 + lane;
-        const uint8_t* src = in + (b >> 1) * HALF_BYTES + r * 128;
+        const int b = task % T::ROW_BLOCKS;
+        const int r = (task / T::ROW_BLOCKS) * 32 + lane;
+        const uint8_t* src = in + (b >> 1) * BOX_BYTES + r * 128;
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -381,7 +405,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
           const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
           rne_words16<FMT>(w, exp2_neg(e), out);
           zero_if_bad(bad, out);
-          scr_s[sf_stage_off(r, b, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+          scr_s[r * T::ROW_BLOCKS + b] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
         } else {
           float v[32];
 #pragma unroll
@@ -397,15 +421,13 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
           }
           const uint64_t idx0 = static_cast<uint64_t>(r0 + r) * static_cast<uint64_t>(p.cols) + (c0 + 32 * b);
           const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, 1, out);
-          scr_s[sf_stage_off(r, b, p.sf_mma)] = static_cast<uint8_t>(sc);
+          scr_s[r * T::ROW_BLOCKS + b] = static_cast<uint8_t>(sc);
         }
         if constexpr (FP4) {
-          // [128 rows][64 B], 64-byte swizzle: 16-B chunk index ^= (row >> 1) & 3
-          *reinterpret_cast<uint4*>(qrow_s + r * 64 + ((b ^ ((r >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
         } else {
-          // [128 rows][128 B], 128-byte swizzle: 16-B chunk index ^= row & 7
-          *reinterpret_cast<uint4*>(qrow_s + r * 128 + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-          *reinterpret_cast<uint4*>(qrow_s + r * 128 + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, 2 * b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, 2 * b + 1, QBR) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
         }
       }
     }
@@ -414,13 +436,13 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     // 4-byte shared loads: a warp reads 128 contiguous bytes of a row.
     if constexpr (DO_COL) {
       if (col_task >= 0) {
-        const int hh = col_task & 1, rb = col_task >> 1;
+        const int hh = col_task % (TC / 64), rb = col_task / (TC / 64);
         const int chk = lane >> 2, wb = (lane & 3) * 4;
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int row = rb * 32 + k;
-          w[k] = *reinterpret_cast<const uint32_t*>(in + hh * HALF_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
+          w[k] = *reinterpret_cast<const uint32_t*>(in + hh * BOX_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
         }
         uint32_t m2 = 0;                       // packed amax of both columns
 #pragma unroll
@@ -439,7 +461,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
             const int e = scale_exp<FMT>(bad ? 0u : abw, p.ceil_mode);
             rne_col32<FMT>(w, half, exp2_neg(e), out);
             zero_if_bad(bad, out);
-            scc_s[sf_stage_off(cl, rb, p.sf_mma)] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+            scc_s[cl * 4 + rb] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
           } else {
             float v[32];
 #pragma unroll
@@ -453,16 +475,13 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
             }
             const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
             const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
-            scc_s[sf_stage_off(cl, rb, p.sf_mma)] = static_cast<uint8_t>(sc);
+            scc_s[cl * 4 + rb] = static_cast<uint8_t>(sc);
           }
           if constexpr (FP4) {
-            // [128 cols][64 B], 64-byte swizzle: 16-B chunk index ^= (col >> 1) & 3
-            *reinterpret_cast<uint4*>(qcol_s + cl * 64 + ((rb ^ ((cl >> 1) & 3)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, rb, QBC) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
           } else {
-            // [128 cols][128 B], 128-byte swizzle: 16-B chunk index ^= col & 7
-            const int c7 = cl & 7;
-            *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb) ^ c7) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-            *reinterpret_cast<uint4*>(qcol_s + cl * 128 + (((2 * rb + 1) ^ c7) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, 2 * rb, QBC) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, 2 * rb + 1, QBC) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
           }
         }
       }
@@ -474,44 +493,53 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       if constexpr (DO_ROW) tma_store_2d(&map_qrow, smem_u32(qrow_s), FP4 ? c0 / 2 : c0, r0);
       if constexpr (DO_COL) tma_store_2d(&map_qcol, smem_u32(qcol_s), FP4 ? r0 / 2 : r0, c0);
       bulk_commit();
-      if (blockIdx.x + (i + NST) * gridDim.x < p.ntiles) { issue(i + NST); issued = i + NST + 1; }
+      if (blockIdx.x + (i + NSTG) * gridDim.x < p.ntiles) { issue(i + NSTG); issued = i + NSTG + 1; }
     }
 
     // ------------------------------------------------------------ scales out
+    // One thread per row (row scales) or per column (column scales) writes
+    // that entity's bytes of this tile in the requested layout.
     if constexpr (!PERTENSOR) {
       if constexpr (DO_ROW) {
-        if (p.sf_mma) {
-          if (tid < 32) {
-            const int kb4 = p.cols / 128;
-            uint8_t* dst = p.s_row + (static_cast<size_t>(r0 / 128) * kb4 + c0 / 128) * 512;
-            reinterpret_cast<uint4*>(dst)[tid] = reinterpret_cast<const uint4*>(scr_s)[tid];
-          }
-        } else if (tid < TILE && r0 + tid < p.rows) {
-          const int kb = p.cols / 32, b0 = c0 / 32;
-          const uint32_t v = reinterpret_cast<const uint32_t*>(scr_s)[tid];
-          uint8_t* dst = p.s_row + static_cast<size_t>(r0 + tid) * kb + b0;
-          if ((kb & 3) == 0 && b0 + 4 <= kb) {
-            *reinterpret_cast<uint32_t*>(dst) = v;
+        if (tid < TR && r0 + tid < p.rows) {
+          const int r = tid, kb = p.cols / 32, b0 = c0 / 32;
+          uint32_t v = 0;
+#pragma unroll
+          for (int b = 0; b < T::ROW_BLOCKS; ++b) v |= static_cast<uint32_t>(scr_s[r * T::ROW_BLOCKS + b]) << (8 * b);
+          uint8_t* dst;
+          bool vec;
+          if (p.sf_mma) {   // full tiles only (rows, cols % 128 == 0)
+            dst = p.s_row + (static_cast<size_t>(r0 / 128) * (p.cols / 128) + c0 / 128) * 512 + (r & 31) * 16 +
+                  ((r >> 5) & 3) * 4 + (c0 & 127) / 32;
+            vec = true;
           } else {
-            for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+            dst = p.s_row + static_cast<size_t>(r0 + r) * kb + b0;
+            vec = (kb % T::ROW_BLOCKS) == 0 && b0 + T::ROW_BLOCKS <= kb;
+          }
+          if (vec) {
+            if constexpr (T::ROW_BLOCKS == 4) *reinterpret_cast<uint32_t*>(dst) = v;
+            else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(v);
+          } else {
+            for (int b = 0; b < T::ROW_BLOCKS && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
           }
         }
       }
       if constexpr (DO_COL) {
-        if (p.sf_mma) {
-          if (tid < 32) {
-            const int rb4 = p.rows / 128;
-            uint8_t* dst = p.s_col + (static_cast<size_t>(c0 / 128) * rb4 + r0 / 128) * 512;
-            reinterpret_cast<uint4*>(dst)[tid] = reinterpret_cast<const uint4*>(scc_s)[tid];
-          }
-        } else if (tid < TILE && c0 + tid < p.cols) {
-          const int kb = p.rows / 32, b0 = r0 / 32;
-          const uint32_t v = reinterpret_cast<const uint32_t*>(scc_s)[tid];
-          uint8_t* dst = p.s_col + static_cast<size_t>(c0 + tid) * kb + b0;
-          if ((kb & 3) == 0 && b0 + 4 <= kb) {
+        if (tid < TC && c0 + tid < p.cols) {
+          const int c = tid, kb = p.rows / 32, b0 = r0 / 32;
+          const uint32_t v = reinterpret_cast<const uint32_t*>(scc_s)[c];
+          if (p.sf_mma) {   // full tiles only
+            const int cc = (c0 & 127) + c;
+            uint8_t* dst = p.s_col + (static_cast<size_t>(c0 / 128) * (p.rows / 128) + r0 / 128) * 512 +
+                           (cc & 31) * 16 + ((cc >> 5) & 3) * 4;
             *reinterpret_cast<uint32_t*>(dst) = v;
           } else {
-            for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+            uint8_t* dst = p.s_col + static_cast<size_t>(c0 + c) * kb + b0;
+            if ((kb & 3) == 0 && b0 + 4 <= kb) {
+              *reinterpret_cast<uint32_t*>(dst) = v;
+            } else {
+              for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+            }
           }
         }
       }
@@ -522,7 +550,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   if (tid == 0) {
     bulk_wait_all();
     if (aborted) {
-      for (int j = i; j < issued; ++j) (void)mbar_wait(smem_u32(&bars[j % NST]), (j / NST) & 1, p.status);
+      for (int j = i; j < issued; ++j) (void)mbar_wait(smem_u32(&bars[j % NSTG]), (j / NSTG) & 1, p.status);
     }
   }
 
@@ -534,7 +562,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     __syncthreads();
     if (tid == 0) {
       uint32_t m = 0;
-      for (int k = 0; k < THREADS / 32; ++k) m = max(m, red[k]);
+      for (int k = 0; k < T::NW; ++k) m = max(m, red[k]);
       const int n = p.hist_len;
       if (p.ring == nullptr) {
         atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), m);
@@ -650,22 +678,32 @@ using namespace mxq_host;
 
 namespace {
 
+constexpr int QTC = MXQ_QUANT_TC;
+constexpr int QNST = MXQ_QUANT_NST;
+
 template <int FMT, int ORIENT, bool PT, bool EXTRA>
 int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
                  cudaStream_t st) {
-  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA>;
-  // stages, two staging tiles, two scale chunks, barriers + reduction (256 B), alignment slack
-  const int smem = NST * IN_STAGE_BYTES + 16384 * 2 + 512 * 2 + 256 + 1024;
-  static bool attr_set[64] = {};
+  using T = TileCfg<QTC, QNST, EXTRA>;
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QTC, QNST>;
+  constexpr bool FP4 = FMT == MXQ_E2M1;
+  constexpr int rowstg = ((TR * (FP4 ? QTC / 2 : QTC)) + 1023) & ~1023;
+  constexpr int colstg = ((QTC * (FP4 ? TR / 2 : TR)) + 1023) & ~1023;
+  // stages, two staging tiles, two scale areas, barriers + reduction (256 B), alignment slack
+  constexpr int smem = QNST * T::IN_BYTES + rowstg + colstg + 512 * 2 + 256 + 1024;
+  static int per_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!attr_set[dev & 63]) {
+  if (!per_sm[dev & 63]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return MXQ_ERR_CUDA;
-    attr_set[dev & 63] = true;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS, smem) != cudaSuccess || n < 1)
+      return MXQ_ERR_CUDA;
+    per_sm[dev & 63] = n;
   }
-  const int grid = std::min(p.ntiles, (EXTRA ? 1 : 2) * sm_count());
-  return launch_pdl(kern, dim3(grid), dim3(THREADS), smem, st, mx, mr, mc, p);
+  const int grid = std::min(p.ntiles, per_sm[dev & 63] * sm_count());
+  return launch_pdl(kern, dim3(grid), dim3(T::THREADS), smem, st, mx, mr, mc, p);
 }
 
 template <bool PT>
@@ -688,25 +726,29 @@ int dispatch(int fmt, int orient, const CUtensorMap& mx, const CUtensorMap& mr, 
 bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E5M2 || f == MXQ_E2M1; }
 bool valid_orient(int o) { return o == MXQ_ROW || o == MXQ_COL || o == MXQ_DUAL; }
 
-// Tensor maps of the tile kernel: input halves, row codes, transposed codes.
+CUtensorMapSwizzle swizzle_for(int pitch) {
+  return pitch >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (pitch == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// Tensor maps of the tile kernel: input boxes (128 rows x 64 bf16), row
+// codes (128 rows x tile-width bytes), transposed codes (tile-width columns x
+// 128 rows of bytes); the staging swizzle follows the staged row pitch.
 int make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, bool fp4, int orient, void* q_row,
               void* q_col, CUtensorMap* mx, CUtensorMap* mr, CUtensorMap* mc) {
-  if (!encode_2d(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, cols, rows, ld * 2, 64, TILE,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, cols, rows, ld * 2, 64, TR, CU_TENSOR_MAP_SWIZZLE_128B))
     return MXQ_ERR_CUDA;
-  const int qb = fp4 ? 64 : 128;
   *mr = *mx;
   *mc = *mx;
   if (orient & MXQ_ROW) {
     const uint64_t inner = fp4 ? cols / 2 : cols;
-    if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qb, TILE,
-                   fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    const int qbr = fp4 ? QTC / 2 : QTC;
+    if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qbr, TR, swizzle_for(qbr)))
       return MXQ_ERR_CUDA;
   }
   if (orient & MXQ_COL) {
     const uint64_t inner = fp4 ? rows / 2 : rows;
-    if (!encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, inner, cols, inner, qb, TILE,
-                   fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    const int qbc = fp4 ? TR / 2 : TR;
+    if (!encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, inner, cols, inner, qbc, QTC, swizzle_for(qbc)))
       return MXQ_ERR_CUDA;
   }
   return MXQ_OK;
@@ -725,7 +767,7 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   if ((orient & MXQ_ROW) && (!q_row || !s_row)) return MXQ_ERR_BAD_ARG;
   if ((orient & MXQ_COL) && (!q_col || !s_col)) return MXQ_ERR_BAD_ARG;
   if (rows <= 0 || cols <= 0 || rows % 32 || cols % 32 || ld < cols) return MXQ_ERR_BAD_SHAPE;
-  if (rows > (1ll << 31) - TILE || cols > (1ll << 31) - TILE) return MXQ_ERR_BAD_SHAPE;
+  if (rows > (1ll << 31) - 256 || cols > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
   if (sf_layout == MXQ_SF_MMA && (rows % 128 || cols % 128)) return MXQ_ERR_BAD_SHAPE;
   if (!aligned16(x) || ld % 8) return MXQ_ERR_MISALIGNED;
   if ((orient & MXQ_ROW) && !aligned16(q_row)) return MXQ_ERR_MISALIGNED;
@@ -740,8 +782,8 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   QuantParams p{};
   p.rows = static_cast<int>(rows);
   p.cols = static_cast<int>(cols);
-  p.tiles_c = static_cast<int>((cols + TILE - 1) / TILE);
-  p.ntiles = p.tiles_c * static_cast<int>((rows + TILE - 1) / TILE);
+  p.tiles_c = static_cast<int>((cols + QTC - 1) / QTC);
+  p.ntiles = p.tiles_c * static_cast<int>((rows + TR - 1) / TR);
   p.ceil_mode = scale_mode == MXQ_SCALE_CEIL;
   p.rounding = rounding;
   p.hadamard = hadamard32 != 0;
@@ -769,7 +811,7 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
   if (ring_state && (hist_len < 1 || hist_idx < 0 || hist_idx >= hist_len)) return MXQ_ERR_BAD_ARG;
   if (rows <= 0 || cols <= 0 || cols % 16) return MXQ_ERR_BAD_SHAPE;
   if ((orient & MXQ_COL) && rows % 16) return MXQ_ERR_BAD_SHAPE;
-  if (rows > (1ll << 31) - TILE || cols > (1ll << 31) - TILE) return MXQ_ERR_BAD_SHAPE;
+  if (rows > (1ll << 31) - 256 || cols > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
   if (!aligned16(x) || ((orient & MXQ_ROW) && !aligned16(x8)) || ((orient & MXQ_COL) && !aligned16(x8T)))
     return MXQ_ERR_MISALIGNED;
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
@@ -781,8 +823,8 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
   QuantParams p{};
   p.rows = static_cast<int>(rows);
   p.cols = static_cast<int>(cols);
-  p.tiles_c = static_cast<int>((cols + TILE - 1) / TILE);
-  p.ntiles = p.tiles_c * static_cast<int>((rows + TILE - 1) / TILE);
+  p.tiles_c = static_cast<int>((cols + QTC - 1) / QTC);
+  p.ntiles = p.tiles_c * static_cast<int>((rows + TR - 1) / TR);
   p.status = status_ptr();
   if (!p.status) return MXQ_ERR_CUDA;
   p.scale = scale;
