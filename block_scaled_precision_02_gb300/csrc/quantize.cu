@@ -40,10 +40,15 @@ namespace mxq {
 #ifndef MXQ_QUANT_NST
 #define MXQ_QUANT_NST 3
 #endif
+// staging buffers for the outgoing code tiles: 2 lets a tile be staged while
+// the previous tile's bulk stores are still reading shared memory
+#ifndef MXQ_QUANT_STG
+#define MXQ_QUANT_STG 2
+#endif
 constexpr int TR = 128;                     // tile rows
 constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
 
-template <int TC, int NSTG, bool EXTRA>
+template <int TC, int NSTG, int NSTAGE_OUT, bool EXTRA>
 struct TileCfg {
   static_assert(TC == 64 || TC == 128, "tile width");
   static constexpr int THREADS = TC * 4;            // one warp per 8 tile columns
@@ -53,8 +58,9 @@ struct TileCfg {
   static constexpr int ROW_TASKS = 4 * ROW_BLOCKS;  // 32 rows x one block each (= NW)
   static constexpr int COL_TASKS = TC / 16;         // 64 columns x 32 rows each (= NW / 2)
   // resident CTAs per SM the registers are budgeted for
+  static constexpr int SMEM_KB = (NSTG * TR * TC * 2 + NSTAGE_OUT * 2 * TR * TC) / 1024;   // approx.
   static constexpr int MIN_BLOCKS = EXTRA ? (TC == 128 ? 1 : 2)
-                                          : (TC == 128 ? 2 : (NSTG == 2 ? 4 : (NSTG == 3 ? 3 : 2)));
+                                          : (TC == 128 ? 2 : (SMEM_KB <= 50 ? 4 : (SMEM_KB <= 70 ? 3 : 2)));
 };
 
 // 16-byte chunk index after the TMA swizzle of a staged row of `pitch`
@@ -286,11 +292,11 @@ __device__ __forceinline__ void pertensor32(const uint32_t (&w)[16], float mult,
 
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
-template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int TC, int NSTG>
-__global__ void __launch_bounds__(TileCfg<TC, NSTG, EXTRA>::THREADS, TileCfg<TC, NSTG, EXTRA>::MIN_BLOCKS)
+template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int TC, int NSTG, int NOUT>
+__global__ void __launch_bounds__(TileCfg<TC, NSTG, NOUT, EXTRA>::THREADS, TileCfg<TC, NSTG, NOUT, EXTRA>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
                    const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
-  using T = TileCfg<TC, NSTG, EXTRA>;
+  using T = TileCfg<TC, NSTG, NOUT, EXTRA>;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
   constexpr bool FP4 = (FMT == MXQ_E2M1);
@@ -302,9 +308,9 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* in_s = smem;
-  uint8_t* qrow_s = in_s + NSTG * T::IN_BYTES;
-  uint8_t* qcol_s = qrow_s + ROWSTG;
-  uint8_t* scr_s = qcol_s + COLSTG;      // [128 rows][ROW_BLOCKS] scale bytes
+  uint8_t* qrow_base = in_s + NSTG * T::IN_BYTES;       // NOUT row staging tiles
+  uint8_t* qcol_base = qrow_base + NOUT * ROWSTG;         // NOUT column staging tiles
+  uint8_t* scr_s = qcol_base + NOUT * COLSTG;   // [128 rows][ROW_BLOCKS] scale bytes
   uint8_t* scc_s = scr_s + 512;          // [TC columns][4] scale bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(scc_s + 512);
   uint32_t* red = reinterpret_cast<uint32_t*>(bars + NSTG);
@@ -365,13 +371,17 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     const uint32_t full_bar = smem_u32(&bars[s]);
     const uint32_t parity = (i / NSTG) & 1;
     // Thread 0 alone waits for the tile's TMA loads (bounded) and for the
-    // previous tile's bulk stores to have left the staging buffers; the rest
-    // of the CTA waits at the barrier instead of spinning.
+    // bulk stores that last used this tile's staging buffers to have read
+    // them out (each tile commits one store group); the rest of the CTA
+    // waits at the barrier instead of spinning.
     bool ok = true;
     if (tid == 0) {
       ok = mbar_wait(full_bar, parity, p.status);
-      bulk_wait_read_all();
+      if constexpr (NOUT == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      else bulk_wait_read_all();
     }
+    uint8_t* qrow_s = qrow_base + (i % NOUT) * ROWSTG;
+    uint8_t* qcol_s = qcol_base + (i % NOUT) * COLSTG;
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     // each thread observes the completed phase itself (acquire); it has
     // completed, so this returns at once
@@ -382,10 +392,10 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     // Shared loads are 16-byte and conflict-free: the TMA 128-byte swizzle
     // puts the 8 rows of a load phase in 8 different bank groups.
     if constexpr (DO_ROW) {
-#pragma unroll 1
+#pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int task = t ? row_task1 : row_task0;
-        if (task < 0) break;
+        if (task < 0) continue;
         const int b = task % T::ROW_BLOCKS;
         const int r = (task / T::ROW_BLOCKS) * 32 + lane;
         const uint8_t* src = in + (b >> 1) * BOX_BYTES + r * 128;
@@ -680,17 +690,18 @@ namespace {
 
 constexpr int QTC = MXQ_QUANT_TC;
 constexpr int QNST = MXQ_QUANT_NST;
+constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA>
 int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
                  cudaStream_t st) {
-  using T = TileCfg<QTC, QNST, EXTRA>;
-  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QTC, QNST>;
+  using T = TileCfg<QTC, QNST, QSTG, EXTRA>;
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QTC, QNST, QSTG>;
   constexpr bool FP4 = FMT == MXQ_E2M1;
   constexpr int rowstg = ((TR * (FP4 ? QTC / 2 : QTC)) + 1023) & ~1023;
   constexpr int colstg = ((QTC * (FP4 ? TR / 2 : TR)) + 1023) & ~1023;
-  // stages, two staging tiles, two scale areas, barriers + reduction (256 B), alignment slack
-  constexpr int smem = QNST * T::IN_BYTES + rowstg + colstg + 512 * 2 + 256 + 1024;
+  // stages, staging tiles, two scale areas, barriers + reduction (256 B), alignment slack
+  constexpr int smem = QNST * T::IN_BYTES + QSTG * (rowstg + colstg) + 512 * 2 + 256 + 1024;
   static int per_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
