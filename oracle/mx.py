@@ -27,6 +27,8 @@ Readings where the pages are silent (each listed in the design notes):
   counter = flat element index); with y' = min(|y|, max) strictly between
   grid neighbours lo < y' < hi, t = floor((y' - lo) / (hi - lo) * 2^32) and
   the magnitude rounds up to hi iff r < t.  The sign is reattached.
+  Option ``SR4``: the same rounding with r = word (index & 3) of the call
+  with counter = index >> 2 (one generator call per four elements).
 * Hadamard: u_j = s_j v_j; butterflies h = 1, 2, 4, 8, 16 in that order in
   float32 round-to-nearest, (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h})
   for (i & h) == 0; then y_j = RN32(u_j * c) with c = RN32(1 / sqrt(32)).
@@ -37,7 +39,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import formats as F
-from .philox import hadamard_signs, sr_draw
+from .philox import hadamard_signs, sr_draw, sr_draw4
 
 K = 32  # MX block size, the same for every MX element type (explainer, section 1)
 
@@ -45,6 +47,7 @@ FLOOR = 0
 CEIL = 1
 RNE = 0
 SR = 1
+SR4 = 2
 ROW = 1
 COL = 2
 DUAL = 3
@@ -129,6 +132,8 @@ def quantize_blocks(vals: np.ndarray, f, mode: int, rounding: int = RNE,
     y = np.where(np.isfinite(y), y, 0.0)
     if rounding == RNE:
         q = F.encode_rne_sat(f, y)
+    elif rounding == SR4:
+        q = stochastic_round(f, y, sr_draw4(sr_seed, flat_idx))
     else:
         q = stochastic_round(f, y, sr_draw(sr_seed, flat_idx))
     q = np.where(bad[..., None], np.uint8(0), q)

@@ -9,6 +9,8 @@ for the 4x32 variant, 10 rounds.
 The method uses it in two places (format-aware fusion article, MXFP4 recipe):
 the stochastic-rounding draw (key = the caller's seed, counter = the element
 index) and the 32 fixed Hadamard signs (key = the sign seed, counter = 0).
+``sr_draw4`` is the four-draws-per-call option of the stochastic-rounding
+draw (counter = index >> 2, word = index & 3).
 """
 
 from __future__ import annotations
@@ -70,6 +72,24 @@ def sr_draw(seed: int, idx: np.ndarray) -> np.ndarray:
     ctr[..., 0] = (idx & np.uint64(MASK)).astype(np.uint32)
     ctr[..., 1] = (idx >> np.uint64(32)).astype(np.uint32)
     return philox4x32_10(ctr, split64(seed))[..., 0]
+
+
+def sr_draw4(seed: int, idx: np.ndarray) -> np.ndarray:
+    """Stochastic-rounding draw, four draws per generator call: word
+    (idx & 3) of Philox-4x32-10 with key = (seed_lo, seed_hi) and counter =
+    (c_lo, c_hi, 0, 0), c = idx >> 2.  Four consecutive indices 4c .. 4c + 3
+    share one call and take its words 0 .. 3 in order.  This is an explicit
+    option of the implementation (the pages fix only that the draws come from
+    Philox keyed by the seed and counted by the element index); with it one
+    generator call serves four elements."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    c = idx >> np.uint64(2)
+    ctr = np.zeros(idx.shape + (4,), dtype=np.uint32)
+    ctr[..., 0] = (c & np.uint64(MASK)).astype(np.uint32)
+    ctr[..., 1] = (c >> np.uint64(32)).astype(np.uint32)
+    words = philox4x32_10(ctr, split64(seed))
+    w = (idx & np.uint64(3)).astype(np.int64)
+    return np.take_along_axis(words, w[..., None], axis=-1)[..., 0]
 
 
 def hadamard_signs(seed: int) -> np.ndarray:

@@ -292,6 +292,53 @@ def test_philox_known_answers():
         assert [int(v) for v in out] == w[6:]
 
 
+def _kat_rows():
+    with open(os.path.join(GOLD, "philox4x32_10_kat.txt")) as fh:
+        return [[int(v, 16) for v in ln.split()] for ln in fh if ln.strip() and not ln.startswith("#")]
+
+
+def test_sr_draw4_known_answers():
+    """Four-draws-per-call option: indices 0..3 with key 0 take words 0..3 of
+    the published counter-0 / key-0 vector, in order."""
+    w = _kat_rows()[0]
+    assert w[:6] == [0] * 6
+    assert [int(v) for v in philox.sr_draw4(0, np.arange(4))] == w[6:]
+
+
+def test_sr_draw4_counter_is_index_over_four():
+    """Index 4c + j takes word j of the call with counter c: word 0 equals the
+    one-draw-per-call draw for index c (itself pinned by the known answers),
+    also when c needs the counter's high word."""
+    for seed in (0, 7, 0x123456789):
+        for c in (0, 1, 5, 2 ** 32 + 5, 2 ** 40 + 3):
+            assert int(philox.sr_draw4(seed, np.array([4 * c]))[0]) == int(philox.sr_draw(seed, np.array([c]))[0])
+    d = philox.sr_draw4(3, np.arange(64))
+    assert len(set(int(v) for v in d)) == 64                     # the four words differ
+
+
+def test_planted_sr4_word_mistake_is_caught():
+    """Taking word 0 for all four indices of a call (a plausible slip) fails
+    the known-answer check above."""
+    w = _kat_rows()[0]
+    wrong = [int(philox.sr_draw(0, np.array([i >> 2]))[0]) for i in range(4)]
+    assert wrong != w[6:]
+
+
+@pytest.mark.parametrize("f", [F.E2M1])
+def test_sr4_unbiased(f):
+    rng = np.random.default_rng(13)
+    y = rng.uniform(-f.max_finite * 0.9, f.max_finite * 0.9, 20)
+    n = 20000
+    idx = np.arange(n, dtype=np.int64)
+    for yi in y:
+        r = philox.sr_draw4(5, idx)
+        s = F.decode(f, mx.stochastic_round(f, np.full(n, yi), r))
+        lo, hi = F.neighbours(f, np.array([abs(yi)]))
+        p = (abs(yi) - lo[0]) / (hi[0] - lo[0]) if hi[0] > lo[0] else 0.0
+        sd = (hi[0] - lo[0]) * math.sqrt(max(p * (1 - p), 1e-12) / n)
+        assert abs(np.mean(s) - yi) <= 5 * sd + 1e-12
+
+
 def test_sr_on_grid_values_are_kept():
     for f in (F.E4M3, F.E5M2, F.E2M1):
         vals, codes = F._positive_grid(f)
