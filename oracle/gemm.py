@@ -12,7 +12,9 @@ higher-precision GEMM.  So the reference is
     C[m, n] = sum_k  dec(a[m, k]) * Xa[m, k/32] * dec(b[n, k]) * Xb[n, k/32]
 
 in float64 (every product is exact), with A [M][K] and B [N][K] both
-K-contiguous (C = A * B^T).
+K-contiguous (C = A * B^T).  Each operand is decoded with its own element
+format: the explainer's FP8 section sets E4M3 (more precise) beside E5M2
+(wider range), so a product may pair an E5M2 gradient with an E4M3 operand.
 
 Gate (reading; the target "max relative error 2e-3 against the float64
 product" made attainable for a bf16 output): for each element,
@@ -30,17 +32,17 @@ import numpy as np
 from .mx import dequantize
 
 
-def reference(a_q, a_s, b_q, b_s, f) -> np.ndarray:
-    """float64 C = dequant(A) @ dequant(B)^T."""
+def reference(a_q, a_s, b_q, b_s, f, fb=None) -> np.ndarray:
+    """float64 C = dequant(A) @ dequant(B)^T; A in format f, B in fb (default f)."""
     A = dequantize(a_q, a_s, f)
-    B = dequantize(b_q, b_s, f)
+    B = dequantize(b_q, b_s, f if fb is None else fb)
     return A @ B.T
 
 
-def reference_rows_cols(a_q, a_s, b_q, b_s, f, rows, cols) -> np.ndarray:
+def reference_rows_cols(a_q, a_s, b_q, b_s, f, rows, cols, fb=None) -> np.ndarray:
     """Sampled reference: C[rows][:, cols] only (rows/cols index arrays)."""
     A = dequantize(np.asarray(a_q)[rows], np.asarray(a_s)[rows], f)
-    B = dequantize(np.asarray(b_q)[cols], np.asarray(b_s)[cols], f)
+    B = dequantize(np.asarray(b_q)[cols], np.asarray(b_s)[cols], f if fb is None else fb)
     return A @ B.T
 
 

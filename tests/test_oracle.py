@@ -434,6 +434,30 @@ def test_gemm_unit_rows_pick_columns():
     assert np.array_equal(ref, 4.0 * deqA[:, cols])
 
 
+def test_gemm_mixed_formats_decode_each_operand():
+    """A in E4M3 times B in E5M2 with unit rows: C[:, n] is a column of A's
+    dequantized values times B's value.  After block scaling B's single
+    non-zero per row is the E5M2 element 1.5 * 2^15, far outside E4M3's
+    range, so decoding B with A's format (a plausible slip) fails."""
+    rng = np.random.default_rng(14)
+    M, N, K = 64, 32, 128
+    a = rng.standard_normal((M, K))
+    A = mx.quantize(a, F.E4M3, mx.ROW)
+    b = np.zeros((N, K))
+    cols = rng.choice(K, N, replace=False)
+    vals = np.array([1.5 * 2.0 ** e for e in rng.integers(-12, 15, N)])
+    b[np.arange(N), cols] = vals
+    B = mx.quantize(b, F.E5M2, mx.ROW)
+    deqA = mx.dequantize(A["q_row"], A["s_row"], F.E4M3)
+    ref = gemm.reference(A["q_row"], A["s_row"], B["q_row"], B["s_row"], F.E4M3, F.E5M2)
+    assert np.array_equal(ref, deqA[:, cols] * vals)
+    wrong = gemm.reference(A["q_row"], A["s_row"], B["q_row"], B["s_row"], F.E4M3)
+    assert not np.array_equal(wrong, ref)
+    sub = gemm.reference_rows_cols(A["q_row"], A["s_row"], B["q_row"], B["s_row"], F.E4M3,
+                                   np.arange(5), np.arange(7), F.E5M2)
+    assert np.array_equal(sub, ref[:5, :7])
+
+
 def test_gemm_pm_one_integer_sums():
     rng = np.random.default_rng(5)
     M, N, K = 32, 32, 256
