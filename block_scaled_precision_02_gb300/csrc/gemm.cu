@@ -7,20 +7,31 @@
 // and accumulate in FP32; gap section 2 -- the blocks must run along the
 // contiguous reduction dimension (both operands K-contiguous, C = A * B^T).
 //
-// Kernel structure (one CTA per SM, persistent over 128 x BN output tiles):
-//  * warp 0      TMA producer: per K step (128 bytes of codes per row) one
-//                128 x 128 B tile of A and one BN x 128 B tile of B with the
-//                128-byte swizzle, plus the matching 512-byte scale chunks
-//                (bulk copies; the quantizer already wrote them in the
-//                tensor-core layout), into a 4-stage ring.
-//  * warp 1      allocates tensor memory; one thread issues tcgen05.cp of the
-//                scale chunks into tensor memory and 4 block-scaled
-//                tcgen05.mma per stage (E4M3/E5M2: kind::mxf8f6f4,
-//                scale_vec::1X, K = 32; E2M1: kind::mxf4, scale_vec::2X,
-//                K = 64), then tcgen05.commit to free the stage.
-//  * warps 2..5  epilogue: tcgen05.ld of the 128 x BN float32 accumulator
-//                (each thread owns one row), conversion, and TMA stores
-//                through two 64-byte-swizzled staging buffers.
+// Two kernels share the warp roles below.
+//  * CTA pair (M and N multiples of 256): clusters of two CTAs on two SMs
+//    compute one 256 x 256 tile with tcgen05.mma.cta_group::2.  Each CTA
+//    holds its own 128 rows of A and one 128-row half of B; the tensor cores
+//    of the pair exchange the B halves, so each SM streams 32 KB of operands
+//    per K step instead of 48 KB.  Scale chunks: each CTA holds its own rows
+//    of A's scales and all 256 rows of B's; one tcgen05.cp.cta_group::2
+//    fills both CTAs' tensor memory from the same offset.
+//  * single CTA (otherwise): 128 x BN tiles, tcgen05.mma.cta_group::1.
+// Roles (one CTA per SM, persistent over output tiles):
+//  * warp 0      TMA producer: per K step (128 bytes of codes per row) the
+//                A and B tiles with the 128-byte swizzle, plus the matching
+//                512-byte scale chunks (the quantizer already wrote them in
+//                the tensor-core layout), into a ring of stages.
+//  * warp 1      allocates tensor memory; one thread (of the pair's first
+//                CTA) issues 4 block-scaled tcgen05.mma per stage (E4M3/E5M2:
+//                kind::mxf8f6f4, scale_vec::1X, K = 32; E2M1: kind::mxf4,
+//                scale_vec::2X, K = 64), then tcgen05.commit to free the
+//                stage (in both CTAs of a pair).  The single-CTA kernel
+//                issues the tcgen05.cp of the scale chunks into tensor memory
+//                from the same thread; the pair kernel leaves them to warp 6,
+//                which runs ahead of the MMAs.
+//  * warps 2..5  epilogue: tcgen05.ld of this CTA's 128 x N float32
+//                accumulator rows (each thread owns one row), conversion,
+//                and TMA stores through two 64-byte-swizzled staging buffers.
 // Every wait is bounded (1 s); on expiry the status word records
 // MXQ_ERR_TIMEOUT, all roles wind down, in-flight copies are awaited (with a
 // limit) and tensor memory is released.
@@ -36,6 +47,7 @@ constexpr int BKB = 128;                 // bytes of codes per row per stage
 constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
+constexpr int PAIR_THREADS = 224;     // pair kernel: the roles above plus warp 6 (scale copies)
 constexpr int STG_BYTES = BM * 64;       // one staging buffer: 128 rows x 64 B
 
 struct Params {
@@ -102,6 +114,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// CTA-pair forms: issued by one thread of the pair's first CTA (alloc and
+// dealloc by one warp of each CTA); shared-memory descriptors and tensor
+// memory addresses name the same offsets in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// arrive on the mbarrier at this offset in both CTAs once the issued work is done
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_self(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+template <bool FP4>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t acc) {
+  if constexpr (FP4) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
@@ -124,6 +179,91 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, int n, int m, uint32_t sf_id) {
   return (sf_id << 4) | (ab_type << 7) | (ab_type << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
+}
+
+// Epilogue of one output tile: drain this CTA's 128 x BN float32
+// accumulator (tensor-memory lanes 0..127, columns 0..BN-1; the thread of
+// lane quarter q and lane `lane` owns row 32 q + lane), call release() once
+// it has been read completely, and store it to C[m0 .., n0 ..] through two
+// 64-byte-swizzled staging buffers (TMA stores issued by `leader`).  All 128
+// epilogue threads take part (named barrier 1).
+template <int BN, typename Release>
+__device__ __forceinline__ void store_tile(uint32_t tmem, int q, int lane, bool leader, int& buf, uint8_t* sOut,
+                                           const CUtensorMap* map_c, int m0, int n0, int out_fp32, Release release) {
+  const int row = q * 32 + lane;
+  if (!out_fp32) {
+    // bf16: drain the whole accumulator row into registers first, so the
+    // MMA warp can start the next tile while this one is written out
+    // (two 32-column loads in flight per wait)
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int c = 0; c < BN / 32; c += 2) {
+      uint32_t v[2][32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v[0]);
+      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + (c + 1) * 32, v[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 b2 =
+              __floats2bfloat162_rn(__uint_as_float(v[h][2 * j]), __uint_as_float(v[h][2 * j + 1]));
+          pk[(c + h) * 16 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    release();
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      named_bar(1, 128);
+      uint8_t* stg = sOut + buf * STG_BYTES;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int phys = j ^ ((row >> 1) & 3);                   // 64-byte swizzle
+        *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
+            make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar(1, 128);
+      if (leader) {
+        tma_store_2d(map_c, smem_u32(stg), n0 + c * 32, m0);
+        bulk_commit();
+      }
+      buf ^= 1;
+    }
+    return;
+  }
+  // float32 output: chunk by chunk
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+    tmem_ld_wait();
+    if (c0 + 32 == BN) {                                         // accumulator fully read
+      tc_fence_before();
+      __syncwarp();
+      release();
+    }
+    for (int h = 0; h < 2; ++h) {
+      if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      named_bar(1, 128);
+      uint8_t* stg = sOut + buf * STG_BYTES;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int phys = j ^ ((row >> 1) & 3);                   // 64-byte swizzle
+        *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
+            make_uint4(v[h * 16 + 4 * j], v[h * 16 + 4 * j + 1], v[h * 16 + 4 * j + 2], v[h * 16 + 4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar(1, 128);
+      if (leader) {
+        tma_store_2d(map_c, smem_u32(stg), n0 + c0 + h * 16, m0);
+        bulk_commit();
+      }
+      buf ^= 1;
+    }
+  }
 }
 
 template <int FMT, int BN>
@@ -279,7 +419,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                                      // tensor-memory lane quarter
-    const int row = q * 32 + lane;                               // row within the tile
     const bool leader = (warp == EPI_WARP0 && lane == 0);
     int t = 0, buf = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++t) {
@@ -289,74 +428,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      if (!p.out_fp32) {
-        // bf16: drain the whole accumulator row into registers first, so the
-        // MMA warp can start the next tile while this one is written out
-        uint32_t pk[BN / 2];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            pk[c * 16 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
+      store_tile<BN>(tmem, q, lane, leader, buf, sOut, &map_c, m0, n0, p.out_fp32, [&] {
         if (lane == 0) mbar_arrive(smem_u32(acc_empty));
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          named_bar(1, 128);
-          uint8_t* stg = sOut + buf * STG_BYTES;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int phys = j ^ ((row >> 1) & 3);               // 64-byte swizzle
-            *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
-                make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
-          }
-          fence_proxy_async_smem();
-          named_bar(1, 128);
-          if (leader) {
-            tma_store_2d(&map_c, smem_u32(stg), n0 + c * 32, m0);
-            bulk_commit();
-          }
-          buf ^= 1;
-        }
-        continue;
-      }
-      // float32 output: chunk by chunk
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
-        tmem_ld_wait();
-        if (c0 + 32 == BN) {                                     // accumulator fully read
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(acc_empty));
-        }
-        for (int h = 0; h < 2; ++h) {
-          if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          named_bar(1, 128);
-          uint8_t* stg = sOut + buf * STG_BYTES;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int phys = j ^ ((row >> 1) & 3);               // 64-byte swizzle
-            *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) =
-                make_uint4(v[h * 16 + 4 * j], v[h * 16 + 4 * j + 1], v[h * 16 + 4 * j + 2], v[h * 16 + 4 * j + 3]);
-          }
-          fence_proxy_async_smem();
-          named_bar(1, 128);
-          if (leader) {
-            tma_store_2d(&map_c, smem_u32(stg), n0 + c0 + h * 16, m0);
-            bulk_commit();
-          }
-          buf ^= 1;
-        }
-      }
+      });
     }
     if (leader) bulk_wait_all();
   }
@@ -365,6 +439,229 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- CTA pair
+// 256 x 256 output tiles per cluster of two CTAs.  CTA rank r of the pair
+// holds rows m0 + 128 r .. of A, rows n0 + 128 r .. of B, A's scale chunks of
+// its own rows and B's of all 256 rows.  The pair's first CTA (rank 0) owns
+// the stage ring's "full" barriers (both CTAs' loads complete on them), the
+// accumulator-empty barrier (all 8 epilogue warps arrive) and issues the
+// tensor-core work (scale copies from warp 6, MMAs from warp 1); its MMA
+// commits arrive on the "empty" and accumulator-full barriers of both CTAs.
+template <int FMT>
+struct PairCfg {
+  static constexpr bool FP4 = FMT == MXQ_E2M1;
+  static constexpr int BN = 256;                        // columns per tile (both CTAs)
+  static constexpr int STAGES = FP4 ? 5 : 6;
+  static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
+  static constexpr int SF_CHUNKS = FP4 ? 2 : 1;         // 512-B chunks per 128 rows per stage
+  static constexpr int SFA_BYTES = 512 * SF_CHUNKS;
+  static constexpr int SFB_BYTES = 2 * SFA_BYTES;       // both 128-row halves of B
+  static constexpr int TX_CTA = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SFA_COLS = 4 * SF_CHUNKS;
+  static constexpr int SFB_COLS = 8 * SF_CHUNKS;
+  static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
+  static constexpr uint32_t AB_TYPE = FMT == MXQ_E4M3 ? 0u : 1u;   // E5M2 = 1; E2M1 in kind::mxf4 = 1
+  static constexpr int SMEM = STAGES * TX_CTA + 2 * STG_BYTES + 256 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
+                    const __grid_constant__ CUtensorMap map_c, const Params p) {
+  using C = PairCfg<FMT>;
+  constexpr int STAGES_P = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                                          // STAGES x A_BYTES
+  uint8_t* sB = sA + STAGES_P * C::A_BYTES;                    // STAGES x B_BYTES
+  uint8_t* sSFA = sB + STAGES_P * C::B_BYTES;                  // STAGES x SFA_BYTES
+  uint8_t* sSFB = sSFA + STAGES_P * C::SFA_BYTES;              // STAGES x SFB_BYTES
+  uint8_t* sOut = sSFB + STAGES_P * C::SFB_BYTES;              // 2 x STG_BYTES (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 2 * STG_BYTES);
+  uint64_t* full = bars;                                       // used in rank 0
+  uint64_t* empty = bars + STAGES_P;
+  uint64_t* acc_full = bars + 2 * STAGES_P;
+  uint64_t* acc_empty = acc_full + 1;                          // used in rank 0
+  uint64_t* drain = acc_full + 2;                              // used in rank 0
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(acc_full + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_full + 3) + 1;
+  volatile int* epi_fail = reinterpret_cast<volatile int*>(acc_full + 3) + 2;
+  uint64_t* sf_full = acc_full + 5;                            // rank 0: a slot's scales are in tensor memory
+  uint64_t* sf_drain = sf_full + STAGES_P;                     // rank 0
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES_P; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);                        // rank 0's producer arrives (with both CTAs' bytes)
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 8);                         // the epilogue warps of both CTAs
+    mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < STAGES_P; ++s) mbar_init(smem_u32(&sf_full[s]), 1);
+    mbar_init(smem_u32(sf_drain), 1);
+    *abort_flag = 0;
+    *epi_fail = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&map_a);
+    prefetch_tensormap(&map_b);
+    prefetch_tensormap(&map_sfa);
+    prefetch_tensormap(&map_sfb);
+    prefetch_tensormap(&map_c);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();                  // barriers of both CTAs initialised, tensor memory allocated in both
+  tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();                 // before any global-memory access
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_sf = tmem + C::BN;                       // column offset of the scale area
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int u = 0;                                               // stage use counter
+      for (int tile = pair; tile < p.ntiles && !*abort_flag; tile += npairs) {
+        const int m0 = (tile / p.tiles_n) * 256 + static_cast<int>(rank) * BM;
+        const int nt = (tile % p.tiles_n) * 256;
+        for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
+          const int s = u % STAGES_P;
+          if (!mbar_wait_suspend(smem_u32(&empty[s]), ((u / STAGES_P) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
+          if (rank == 0 && blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
+          const uint32_t fb = cluster_map(smem_u32(&full[s]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::TX_CTA);
+          tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, m0);
+          tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, nt + static_cast<int>(rank) * 128);
+          // scale maps: one 512-B chunk per row, chunk (rb, kc) at row rb * kb4 + kc
+          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &map_sfa, fb, 0, (m0 / 128) * p.kb4 + kb * C::SF_CHUNKS);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES), &map_sfb, fb, 0,
+                             (nt / 128 + h) * p.kb4 + kb * C::SF_CHUNKS);
+        }
+      }
+      // rank 0: make sure no copy of either CTA is still landing when the pair ends
+      // (rank 1 is held at the final cluster barrier until this has finished)
+      if (rank == 0) {
+        for (int s = 0; s < STAGES_P && u > 0; ++s) {
+          int last = u - 1 - ((u - 1 - s) % STAGES_P + STAGES_P) % STAGES_P;
+          if (last >= 0 && last % STAGES_P == s) (void)mbar_wait_suspend(smem_u32(&full[s]), (last / STAGES_P) & 1, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    // The tensor pipe takes only a few instructions ahead, so every cycle
+    // this thread spends elsewhere can idle it: it waits for a slot's scales
+    // (copied by warp 6, which runs ahead) and issues the four MMAs only.
+    if (lane == 0 && rank == 0) {
+      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      uint32_t idesc[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(C::AB_TYPE, C::BN, 2 * BM, C::FP4 ? (kk & 1) * 2 : kk);
+      const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
+      bool ok = true;
+      int s = 0, ph = 0;
+      for (int t = 0; t < my_tiles && ok && !*abort_flag; ++t) {
+        if (!mbar_wait_suspend(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait_suspend(smem_u32(&sf_full[s]), ph, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_sf + s * C::SF_COLS_STAGE;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint64_t ad = a_desc0 + ((s * C::A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + ((s * C::B_BYTES) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
+            const uint32_t sfb = C::FP4 ? sfb_t + 8 * (kk >> 1) : sfb_t;
+            tc_mma_pair<C::FP4>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+          }
+          tc_commit_pair_both(smem_u32(&empty[s]));            // stage free in both CTAs
+          if (++s == STAGES_P) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair_both(smem_u32(acc_full));                // both halves of the accumulator ready
+      }
+      if (!ok) *abort_flag = 1;
+      tc_commit_pair_self(smem_u32(drain));
+      (void)mbar_wait_suspend(smem_u32(drain), 0, p.status);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ scale copies (rank 0)
+    // Per stage: A's chunks and both halves of B's into the slot's own
+    // tensor-memory columns (one tcgen05.cp.cta_group::2 fills both CTAs),
+    // then a commit that tells the MMA issuer they have landed.  A slot is
+    // rewritten only after its stage was refilled, i.e. after the MMAs that
+    // read its previous scales completed.
+    if (lane == 0 && rank == 0) {
+      const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 0, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
+      const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
+      const int total = my_tiles * p.kblocks;
+      int s = 0, ph = 0;
+      for (int u = 0; u < total && !*abort_flag; ++u) {
+        if (!mbar_wait_suspend(smem_u32(&full[s]), ph, p.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t sfa_t = tmem_sf + s * C::SF_COLS_STAGE;
+#pragma unroll
+        for (int c = 0; c < C::SF_CHUNKS; ++c)
+          tc_cp_sf_pair(sfa_t + 4 * c, sfa_desc0 + ((s * C::SFA_BYTES + c * 512) >> 4));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < C::SF_CHUNKS; ++c)
+            tc_cp_sf_pair(sfa_t + C::SFA_COLS + 8 * c + 4 * hh,
+                          sfb_desc0 + ((s * C::SFB_BYTES + hh * C::SFA_BYTES + c * 512) >> 4));
+        tc_commit_pair_self(smem_u32(&sf_full[s]));
+        if (++s == STAGES_P) { s = 0; ph ^= 1; }
+      }
+      tc_commit_pair_self(smem_u32(sf_drain));                // no copy in flight at exit
+      (void)mbar_wait_suspend(smem_u32(sf_drain), 0, p.status);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const bool leader = (warp == EPI_WARP0 && lane == 0);
+    const uint32_t acc_empty_r0 = cluster_map(smem_u32(acc_empty), 0);
+    int t = 0, buf = 0;
+    for (int tile = pair; tile < p.ntiles; tile += npairs, ++t) {
+      const int m0 = (tile / p.tiles_n) * 256 + static_cast<int>(rank) * BM;
+      const int n0 = (tile % p.tiles_n) * 256;
+      if (!mbar_wait_suspend(smem_u32(acc_full), t & 1, p.status)) *epi_fail = 1;
+      named_bar(1, 128);
+      if (*epi_fail) { *abort_flag = 1; break; }
+      tc_fence_after();
+      store_tile<C::BN>(tmem, q, lane, leader, buf, sOut, &map_c, m0, n0, p.out_fp32, [&] {
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(smem_u32(acc_empty));
+          else mbar_arrive_remote(acc_empty_r0);
+        }
+      });
+    }
+    if (leader) bulk_wait_all();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();                  // rank 0's tensor-core work on rank 1's memory has finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
   }
 }
 
@@ -422,6 +719,99 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
   return launch_pdl(kern, dim3(grid), dim3(THREADS), Cf::SMEM, st, ma, mb, mc, p);
 }
 
+// Co-resident clusters of two for the pair kernel (cached per device and
+// format); 0 if the device cannot hold one.
+template <int FMT>
+int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
+              int smem) {
+  static int cache[64] = {};
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cache[dev & 63]) return cache[dev & 63];
+  if (!attr_set[dev & 63]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    attr_set[dev & 63] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sm_count() / 2));
+  cfg.blockDim = dim3(mxq::gemm::PAIR_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[dev & 63] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
+}
+
+template <int FMT>
+int launch_pair(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
+                int64_t K, void* c, int out_fp32, int pairs, cudaStream_t st) {
+  using namespace mxq::gemm;
+  using Cf = PairCfg<FMT>;
+  const int64_t kbytes = Cf::FP4 ? K / 2 : K;
+  const int64_t kb4 = K / 128;
+  CUtensorMap ma, mb, msa, msb, mc;
+  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, kbytes, M, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXQ_ERR_CUDA;
+  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, kbytes, N, kbytes, BKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXQ_ERR_CUDA;
+  // scales in the tensor-core layout: one 512-byte chunk (128 x 32-bit words) per row
+  if (!encode_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_s, 128, (M / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MXQ_ERR_CUDA;
+  if (!encode_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_s, 128, (N / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MXQ_ERR_CUDA;
+  if (out_fp32) {
+    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M, N * 4, 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MXQ_ERR_CUDA;
+  } else {
+    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, N, M, N * 2, 32, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MXQ_ERR_CUDA;
+  }
+  Params p{};
+  p.a_s = a_s;
+  p.b_s = b_s;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.tiles_m = static_cast<int>(M / 256);
+  p.tiles_n = static_cast<int>(N / 256);
+  p.ntiles = p.tiles_m * p.tiles_n;
+  p.kblocks = static_cast<int>(kbytes / BKB);
+  p.kb4 = static_cast<int>(kb4);
+  p.out_fp32 = out_fp32;
+  p.status = status_ptr();
+  p.stall_u = take_test_stall(2) ? 0 : -1;
+  if (!p.status) return MXQ_ERR_CUDA;
+  const int grid = 2 * std::min(p.ntiles, pairs);
+  return launch_pdl_cluster(mx_gemm_pair_kernel<FMT>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb,
+                            mc, p);
+}
+
+// The pair kernel for M and N multiples of 256 (when the device can hold it),
+// else the single-CTA kernel.
+template <int FMT>
+int dispatch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
+             int64_t K, void* c, int out_fp32, cudaStream_t st) {
+  if (M % 256 == 0 && N % 256 == 0) {
+    const int pairs = max_pairs<FMT>(mxq::gemm::mx_gemm_pair_kernel<FMT>, mxq::gemm::PairCfg<FMT>::SMEM);
+    if (pairs > 0) return launch_pair<FMT>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, pairs, st);
+  }
+  return (N % 256 == 0) ? launch<FMT, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st)
+                        : launch<FMT, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
+}
+
 }  // namespace
 
 extern "C" int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M,
@@ -436,13 +826,9 @@ extern "C" int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q, co
     return MXQ_ERR_MISALIGNED;
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
   auto st = static_cast<cudaStream_t>(stream);
-  const bool n256 = (N % 256) == 0;
   switch (fmt) {
-    case MXQ_E4M3: return n256 ? launch<MXQ_E4M3, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st)
-                               : launch<MXQ_E4M3, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
-    case MXQ_E5M2: return n256 ? launch<MXQ_E5M2, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st)
-                               : launch<MXQ_E5M2, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
-    default: return n256 ? launch<MXQ_E2M1, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st)
-                         : launch<MXQ_E2M1, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
+    case MXQ_E4M3: return dispatch<MXQ_E4M3>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
+    case MXQ_E5M2: return dispatch<MXQ_E5M2>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
+    default: return dispatch<MXQ_E2M1>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
   }
 }

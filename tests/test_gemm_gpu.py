@@ -35,13 +35,17 @@ def gpu_gemm(lib, aq, as_, bq, bs, fmt, out_dtype=torch.bfloat16):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
-def test_unit_rows_select_columns_exactly(lib, fmt):
+@pytest.mark.parametrize("mn", [(128, 256), (256, 512), (512, 256)])
+def test_unit_rows_select_columns_exactly(lib, fmt, mn):
     """B row n holds a single non-zero at column perm[n]: C[:, n] is a scaled
     copy of one dequantized column of A (exact in bf16), so the scale mapping
-    of both operands is checked bit for bit."""
+    of both operands is checked bit for bit.  M = 128 runs the single-CTA
+    kernel; M, N multiples of 256 run the CTA-pair kernel (both CTAs' rows,
+    both halves of B)."""
     f = FMTS[fmt]
     rng = np.random.default_rng(1)
-    M, N, K = 128, 256, 512
+    M, N = mn
+    K = 512
     a = rng.standard_normal((M, K)) * np.exp2(rng.integers(-6, 6, size=(M, K // 32))).repeat(32, 1)
     aq, as_ = oracle_operand(a, fmt)
     perm = rng.permutation(K)[:N]
@@ -54,7 +58,8 @@ def test_unit_rows_select_columns_exactly(lib, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
-@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 1024), (384, 384, 512), (128, 128, 2048)])
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 1024), (384, 384, 512), (128, 128, 2048),
+                                 (768, 512, 768), (256, 256, 4096)])
 def test_random_gemm_gate(lib, fmt, mnk):
     M, N, K = mnk
     a = f64(inputs.activations(M, K, seed=0))
