@@ -178,15 +178,16 @@ def source_sha(*names):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, sha: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def traffic_for(kernel: str, sha: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when the kernel source changed since the counters were
+    taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    e = d.get(kernel)
+    e = d.get(f"{kernel} {workload}")
     if not e or e.get("source_sha") != sha:
         return None
     return e.get("bytes_per_launch")
@@ -263,7 +264,7 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
                           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(pk, 1),
                                        "unit": "TFLOP/s", "frac": round(tf / pk, 4),
                                        "peak_source": f"bf16 burst x {RATIO['e4m3']} ({peak_src})",
-                                       "traffic": traffic_for("mx_gemm_kernel", source_sha("gemm.cu"))}})
+                                       "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"), name)}})
     return n
 
 
@@ -276,6 +277,11 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
     for _ in range(3):
         g5 = fp4q()
     ms_q5 = timed(fp4q, args.steps)
+    # the same quantize with the four-draws-per-call option
+    fp4q4 = lambda: q(G5, "e2m1", "floor", "row", rounding="sr4", hadamard32=True, sr_key=0, hadamard_seed=7)
+    for _ in range(3):
+        fp4q4()
+    ms_q5b = timed(fp4q4, args.steps)
     b5 = q(B5, "e2m1", "floor", "row", hadamard32=True, hadamard_seed=7)
     fn5 = lambda: mxq.mx_gemm(g5[0], g5[1], b5[0], b5[1], "e2m1")
     for _ in range(3):
@@ -287,8 +293,9 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
                       "roofline": {"bound": "tensor", "achieved": round(tf5, 1), "peak": round(pk5, 1),
                                    "unit": "TFLOP/s", "frac": round(tf5 / pk5, 4),
                                    "peak_source": f"bf16 burst x {RATIO['e2m1']} ({peak_src})",
-                                   "traffic": traffic_for("mx_gemm_kernel", source_sha("gemm.cu"))}})
-    return ms_q5, 2 * args.steps
+                                   "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"),
+                                                          "mxfp4_4096x4096x14336")}})
+    return (ms_q5, ms_q5b), 3 * args.steps
 
 
 def pertensor_part(args, mxq, X, timed):
@@ -526,7 +533,7 @@ def run_ours(args, rank, world):
                    "isolated_launch_note": "one launch after an L2 flush (256 MiB written then read back), event-timed"},
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(ach / hbm, 4), "peak_source": f"hbm_gbs ({peak_src})",
-                     "traffic": traffic_for("quant_tiles_kernel", source_sha("quantize.cu")),
+                     "traffic": traffic_for("quant_tiles_kernel", source_sha("quantize.cu"), "dual_e4m3_floor_8192x4096"),
                      "algorithmic_bytes_per_launch": mx_quant_bytes(M, K)},
         "clocks": clocks,
         "e2e": {"value": round(step_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -537,7 +544,9 @@ def run_ours(args, rank, world):
         "rows": {
             "pertensor_fp8_ring_4096x14336_dual": hbm_row(b3, ms3, hbm),
             "mxfp4_hadamard_sr_quantize_4096x14336": hbm_row(
-                b_q5, ms_q5, hbm, "one Philox-4x32-10 draw per element: integer-ALU bound"),
+                b_q5, ms_q5[0], hbm, "one Philox-4x32-10 draw per element: integer-ALU bound"),
+            "mxfp4_hadamard_sr4_quantize_4096x14336": hbm_row(
+                b_q5, ms_q5[1], hbm, "option SR4: four draws per Philox-4x32-10 call"),
             "small_rowwise_256x512": {"quantize_us": round(ms1q * 1e3, 2), "dequantize_us": round(ms1d * 1e3, 2)},
         },
         "cpu_baseline": cpu,
