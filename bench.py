@@ -244,16 +244,21 @@ def oracle_gemm_baseline(budget_s: float = 6.0):
 # ---------------------------------------------------------------- measured rows besides the headline
 def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     """MXFP8 GEMMs 8192x4096x4096 and 8192x14336x4096 on operands from our
-    quantizer (A = the activation quantized by the headline step)."""
+    quantizer (A = the activation quantized by the headline step), and the
+    mixed-format product of the headline's E5M2 gradient with the E4M3
+    weights."""
     aq, as_, _, _ = outs[0]
     M, K = 8192, 4096
     W, W2 = X["W"], X["W2"]
     wq, ws, _, _ = q(W, "e4m3", "floor", "row")
     w2q, w2s, _, _ = q(W2, "e4m3", "floor", "row")
+    gq, gs, _, _ = outs[2]                 # the E5M2 gradient of the headline step (row copy)
     n = 0
-    for name, (bq, bs, N) in {"mxfp8_8192x4096x4096": (wq, ws, 4096),
-                              "mxfp8_8192x14336x4096": (w2q, w2s, 14336)}.items():
-        fn = lambda bq=bq, bs=bs: mxq.mx_gemm(aq, as_, bq, bs, "e4m3")
+    for name, (a2, a2s, fa, bq, bs, N) in {
+            "mxfp8_8192x4096x4096": (aq, as_, "e4m3", wq, ws, 4096),
+            "mxfp8_8192x14336x4096": (aq, as_, "e4m3", w2q, w2s, 14336),
+            "mxfp8_mixed_e5m2_x_e4m3_8192x4096x4096": (gq, gs, "e5m2", wq, ws, 4096)}.items():
+        fn = lambda a2=a2, a2s=a2s, fa=fa, bq=bq, bs=bs: mxq.mx_gemm(a2, a2s, bq, bs, fa, b_fmt="e4m3")
         for _ in range(max(3, args.warmup)):
             fn()
         ms = timed(fn, args.steps)

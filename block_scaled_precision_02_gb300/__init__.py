@@ -25,13 +25,13 @@ LIB_PATH = os.path.join(HERE, "libmxq.so")
 E4M3, E5M2, E2M1 = 0, 1, 2
 ROW, COL, DUAL = 1, 2, 3
 FLOOR_OCP, CEIL = 0, 1
-RNE, SR = 0, 1
+RNE, SR, SR4 = 0, 1, 2
 SF_CANONICAL, SF_MMA = 0, 1
 
 _FMT = {"e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1, E4M3: E4M3, E5M2: E5M2, E2M1: E2M1}
 _ORIENT = {"row": ROW, "col": COL, "dual": DUAL, ROW: ROW, COL: COL, DUAL: DUAL}
 _SCALE = {"floor": FLOOR_OCP, "floor_ocp": FLOOR_OCP, "ceil": CEIL, FLOOR_OCP: FLOOR_OCP, CEIL: CEIL}
-_ROUND = {"rne": RNE, "sr": SR, "stochastic": SR, RNE: RNE, SR: SR}
+_ROUND = {"rne": RNE, "sr": SR, "stochastic": SR, "sr4": SR4, RNE: RNE, SR: SR, SR4: SR4}
 _SF = {"canonical": SF_CANONICAL, "mma": SF_MMA, SF_CANONICAL: SF_CANONICAL, SF_MMA: SF_MMA}
 
 _lib = None
@@ -58,13 +58,14 @@ def load() -> ctypes.CDLL:
     L.mxq_dequantize.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
     L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
     L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
+    L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
     L.mxq_last_device_status.argtypes = [vp]
     L.mxq_strerror.argtypes = [i32]
     L.mxq_strerror.restype = ctypes.c_char_p
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
-    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_sf_to_mma",
+    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32
     _lib = L
@@ -190,17 +191,24 @@ def ring_state_new(hist_len: int = 16, device="cuda") -> torch.Tensor:
 
 # --------------------------------------------------------------------------- GEMM
 def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.Tensor, fmt="e4m3",
-            out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None) -> torch.Tensor:
+            out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None, b_fmt=None) -> torch.Tensor:
     """C = A * B^T from MX operands (A [M][K], B [N][K] codes, scales in the
-    MMA layout).  Returns bf16 (or float32) [M][N]."""
+    MMA layout).  ``fmt`` is A's element format and B's unless ``b_fmt`` is
+    given (E4M3 and E5M2 mix; E2M1 pairs with E2M1).  Returns bf16 (or
+    float32) [M][N]."""
     f = _FMT[fmt]
+    fb = f if b_fmt is None else _FMT[b_fmt]
     M = a_q.shape[0]
     N = b_q.shape[0]
     if K is None:
         K = a_q.shape[1] * (2 if f == E2M1 else 1)
     c = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
-    rc = load().mxq_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout], _ptr(c),
-                         int(out_dtype == torch.float32), _stream(a_q.device))
+    if fb == f:
+        rc = load().mxq_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout], _ptr(c),
+                             int(out_dtype == torch.float32), _stream(a_q.device))
+    else:
+        rc = load().mxq_gemm_mixed(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, _SF[sf_layout],
+                                   _ptr(c), int(out_dtype == torch.float32), _stream(a_q.device))
     _check(rc, "mxq_gemm")
     return c
 

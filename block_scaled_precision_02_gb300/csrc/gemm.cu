@@ -59,6 +59,7 @@ struct Params {
   int kb4;            // 512-byte scale chunks per 128 rows (K / 128)
   int out_fp32;
   int* status;
+  uint32_t a_type, b_type;   // element type codes of the instruction descriptor
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
 
@@ -172,12 +173,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor of the block-scaled MMA: A/B element type codes at
-// bits 7-9 / 10-12, K-major operands, N >> 3 at bits 17-22, scale type UE8M0
-// (bit 23), M >> 4 at bits 24-28, scale-factor byte selectors for B (bits 4-5)
-// and A (bits 29-30).
-__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, int n, int m, uint32_t sf_id) {
-  return (sf_id << 4) | (ab_type << 7) | (ab_type << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+// Instruction descriptor of the block-scaled MMA: A and B element type codes
+// at bits 7-9 and 10-12 (kind::mxf8f6f4: E4M3 0, E5M2 1; kind::mxf4: E2M1 1),
+// K-major operands, N >> 3 at bits 17-22, scale type UE8M0 (bit 23), M >> 4
+// at bits 24-28, scale-factor byte selectors for B (bits 4-5) and A (29-30).
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t a_type, uint32_t b_type, int n, int m, uint32_t sf_id) {
+  return (sf_id << 4) | (a_type << 7) | (b_type << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
 }
 
@@ -266,9 +267,9 @@ __device__ __forceinline__ void store_tile(uint32_t tmem, int q, int lane, bool 
   }
 }
 
-template <int FMT, int BN>
+template <bool FP4_, int BN>
 struct Cfg {
-  static constexpr bool FP4 = FMT == MXQ_E2M1;
+  static constexpr bool FP4 = FP4_;
   static constexpr int A_BYTES = BM * BKB;
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int SF_CHUNKS = FP4 ? 2 : 1;         // 512-B chunks per 128 rows per stage
@@ -284,15 +285,14 @@ struct Cfg {
   static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
-  static constexpr uint32_t AB_TYPE = FMT == MXQ_E4M3 ? 0u : (FMT == MXQ_E5M2 ? 1u : 1u);  // E2M1 in kind::mxf4 is 1
   static constexpr int SMEM = STAGES * (STAGE_BYTES + SFA_BYTES + SFB_BYTES) + 2 * STG_BYTES + 256 + 1024;
 };
 
-template <int FMT, int BN>
+template <bool FP4, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = Cfg<FMT, BN>;
+  using C = Cfg<FP4, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                                          // STAGES x A_BYTES
@@ -376,7 +376,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
       uint32_t idesc[4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(C::AB_TYPE, BN, BM, C::FP4 ? (kk & 1) * 2 : kk);
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(p.a_type, p.b_type, BN, BM, C::FP4 ? (kk & 1) * 2 : kk);
       int u = 0, t = 0;
       for (int tile = blockIdx.x; tile < p.ntiles && !*abort_flag; tile += gridDim.x, ++t) {
         if (!mbar_wait(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
@@ -450,9 +450,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // accumulator-empty barrier (all 8 epilogue warps arrive) and issues the
 // tensor-core work (scale copies from warp 6, MMAs from warp 1); its MMA
 // commits arrive on the "empty" and accumulator-full barriers of both CTAs.
-template <int FMT>
+template <bool FP4_>
 struct PairCfg {
-  static constexpr bool FP4 = FMT == MXQ_E2M1;
+  static constexpr bool FP4 = FP4_;
   static constexpr int BN = 256;                        // columns per tile (both CTAs)
   static constexpr int STAGES = FP4 ? 5 : 6;
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
@@ -466,17 +466,16 @@ struct PairCfg {
   static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
-  static constexpr uint32_t AB_TYPE = FMT == MXQ_E4M3 ? 0u : 1u;   // E5M2 = 1; E2M1 in kind::mxf4 = 1
   static constexpr int SMEM = STAGES * TX_CTA + 2 * STG_BYTES + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int FMT>
+template <bool FP4>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
                     const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = PairCfg<FMT>;
+  using C = PairCfg<FP4>;
   constexpr int STAGES_P = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -571,7 +570,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
       uint32_t idesc[4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(C::AB_TYPE, C::BN, 2 * BM, C::FP4 ? (kk & 1) * 2 : kk);
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(p.a_type, p.b_type, C::BN, 2 * BM, C::FP4 ? (kk & 1) * 2 : kk);
       const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
       bool ok = true;
       int s = 0, ph = 0;
@@ -673,11 +672,11 @@ using namespace mxq_host;
 
 namespace {
 
-template <int FMT, int BN>
+template <bool FP4, int BN>
 int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-           int64_t K, void* c, int out_fp32, cudaStream_t st) {
+           int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, cudaStream_t st) {
   using namespace mxq::gemm;
-  using Cf = Cfg<FMT, BN>;
+  using Cf = Cfg<FP4, BN>;
   const int64_t kbytes = Cf::FP4 ? K / 2 : K;
   CUtensorMap ma, mb, mc;
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, kbytes, M, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -704,9 +703,11 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
   p.kb4 = static_cast<int>(K / 128);
   p.out_fp32 = out_fp32;
   p.status = status_ptr();
+  p.a_type = a_type;
+  p.b_type = b_type;
   p.stall_u = take_test_stall(2) ? 0 : -1;
   if (!p.status) return MXQ_ERR_CUDA;
-  auto kern = mx_gemm_kernel<FMT, BN>;
+  auto kern = mx_gemm_kernel<FP4, BN>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -720,8 +721,8 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
 }
 
 // Co-resident clusters of two for the pair kernel (cached per device and
-// format); 0 if the device cannot hold one.
-template <int FMT>
+// kernel); 0 if the device cannot hold one.
+template <bool FP4>
 int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
               int smem) {
   static int cache[64] = {};
@@ -753,11 +754,11 @@ int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, C
   return n > 0 ? n : 0;
 }
 
-template <int FMT>
+template <bool FP4>
 int launch_pair(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-                int64_t K, void* c, int out_fp32, int pairs, cudaStream_t st) {
+                int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, int pairs, cudaStream_t st) {
   using namespace mxq::gemm;
-  using Cf = PairCfg<FMT>;
+  using Cf = PairCfg<FP4>;
   const int64_t kbytes = Cf::FP4 ? K / 2 : K;
   const int64_t kb4 = K / 128;
   CUtensorMap ma, mb, msa, msb, mc;
@@ -792,43 +793,59 @@ int launch_pair(const void* a_q, const uint8_t* a_s, const void* b_q, const uint
   p.kb4 = static_cast<int>(kb4);
   p.out_fp32 = out_fp32;
   p.status = status_ptr();
+  p.a_type = a_type;
+  p.b_type = b_type;
   p.stall_u = take_test_stall(2) ? 0 : -1;
   if (!p.status) return MXQ_ERR_CUDA;
   const int grid = 2 * std::min(p.ntiles, pairs);
-  return launch_pdl_cluster(mx_gemm_pair_kernel<FMT>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb,
+  return launch_pdl_cluster(mx_gemm_pair_kernel<FP4>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb,
                             mc, p);
 }
 
 // The pair kernel for M and N multiples of 256 (when the device can hold it),
 // else the single-CTA kernel.
-template <int FMT>
+template <bool FP4>
 int dispatch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-             int64_t K, void* c, int out_fp32, cudaStream_t st) {
+             int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, cudaStream_t st) {
   if (M % 256 == 0 && N % 256 == 0) {
-    const int pairs = max_pairs<FMT>(mxq::gemm::mx_gemm_pair_kernel<FMT>, mxq::gemm::PairCfg<FMT>::SMEM);
-    if (pairs > 0) return launch_pair<FMT>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, pairs, st);
+    const int pairs = max_pairs<FP4>(mxq::gemm::mx_gemm_pair_kernel<FP4>, mxq::gemm::PairCfg<FP4>::SMEM);
+    if (pairs > 0) return launch_pair<FP4>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, pairs, st);
   }
-  return (N % 256 == 0) ? launch<FMT, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st)
-                        : launch<FMT, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
+  return (N % 256 == 0) ? launch<FP4, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, st)
+                        : launch<FP4, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, st);
+}
+
+// Element type code of the block-scaled MMA's instruction descriptor.
+uint32_t mma_type(int fmt) { return fmt == MXQ_E4M3 ? 0u : 1u; }   // E5M2: 1 (mxf8f6f4); E2M1: 1 (mxf4)
+
+int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s, int b_fmt,
+                 int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32, void* stream) {
+  if (!a_q || !a_s || !b_q || !b_s || !c) return MXQ_ERR_BAD_ARG;
+  for (int f : {a_fmt, b_fmt})
+    if (f != MXQ_E4M3 && f != MXQ_E5M2 && f != MXQ_E2M1) return MXQ_ERR_BAD_ARG;
+  // E2M1 pairs only with E2M1 (kind::mxf4 takes packed FP4 for both operands)
+  if ((a_fmt == MXQ_E2M1) != (b_fmt == MXQ_E2M1)) return MXQ_ERR_UNSUPPORTED;
+  if (sf_layout != MXQ_SF_MMA) return sf_layout == MXQ_SF_CANONICAL ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
+  const bool fp4 = a_fmt == MXQ_E2M1;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % (fp4 ? 256 : 128)) return MXQ_ERR_BAD_SHAPE;
+  if (M > (1ll << 31) - 256 || N > (1ll << 31) - 256 || K > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
+  if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_s) || !aligned16(b_s) || !aligned16(c))
+    return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  auto st = static_cast<cudaStream_t>(stream);
+  return fp4 ? dispatch<true>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, mma_type(a_fmt), mma_type(b_fmt), st)
+             : dispatch<false>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, mma_type(a_fmt), mma_type(b_fmt), st);
 }
 
 }  // namespace
 
 extern "C" int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M,
                         int64_t N, int64_t K, int fmt, int sf_layout, void* c, int out_fp32, void* stream) {
-  if (!a_q || !a_s || !b_q || !b_s || !c) return MXQ_ERR_BAD_ARG;
-  if (fmt != MXQ_E4M3 && fmt != MXQ_E5M2 && fmt != MXQ_E2M1) return MXQ_ERR_BAD_ARG;
-  if (sf_layout != MXQ_SF_MMA) return sf_layout == MXQ_SF_CANONICAL ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % (fmt == MXQ_E2M1 ? 256 : 128))
-    return MXQ_ERR_BAD_SHAPE;
-  if (M > (1ll << 31) - 256 || N > (1ll << 31) - 256 || K > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
-  if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_s) || !aligned16(b_s) || !aligned16(c))
-    return MXQ_ERR_MISALIGNED;
-  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
-  auto st = static_cast<cudaStream_t>(stream);
-  switch (fmt) {
-    case MXQ_E4M3: return dispatch<MXQ_E4M3>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
-    case MXQ_E5M2: return dispatch<MXQ_E5M2>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
-    default: return dispatch<MXQ_E2M1>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, st);
-  }
+  return gemm_checked(a_q, a_s, fmt, b_q, b_s, fmt, M, N, K, sf_layout, c, out_fp32, stream);
+}
+
+extern "C" int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
+                              int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32,
+                              void* stream) {
+  return gemm_checked(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout, c, out_fp32, stream);
 }

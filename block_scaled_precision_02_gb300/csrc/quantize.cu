@@ -139,6 +139,14 @@ __device__ __forceinline__ uint32_t sr_draw(uint64_t idx, uint32_t k0, uint32_t 
   return philox4x32_10(u32x4{static_cast<uint32_t>(idx), static_cast<uint32_t>(idx >> 32), 0u, 0u}, k0, k1).x;
 }
 
+// Four draws per call: word (idx & 3) of the call with counter idx >> 2.
+__device__ __forceinline__ uint32_t sr_draw4(uint64_t idx, uint32_t k0, uint32_t k1) {
+  const uint64_t c = idx >> 2;
+  const u32x4 w = philox4x32_10(u32x4{static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u}, k0, k1);
+  const uint32_t j = static_cast<uint32_t>(idx) & 3u;
+  return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+}
+
 constexpr float kHadC = 0.17677669529663688f;  // float32 nearest 1/sqrt(32)
 
 // Fixed-sign 32-point Hadamard of one block held by one thread:
@@ -256,7 +264,24 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
   const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
   const float m = exp2_neg(e);
   float y[32];
-  if (EXTRA && p.rounding == MXQ_SR) {
+  if (EXTRA && p.rounding == MXQ_SR4 && istep == 1) {
+    // a row block: 32 consecutive indices from a multiple of 32, so the
+    // eight calls with counters idx0/4 .. idx0/4 + 7 give all 32 draws
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t c = (idx0 >> 2) + k;
+      const u32x4 w =
+          philox4x32_10(u32x4{static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u}, p.sr_k0, p.sr_k1);
+      y[4 * k] = sr_round<FMT>(__fmul_rn(v[4 * k], m), w.x);
+      y[4 * k + 1] = sr_round<FMT>(__fmul_rn(v[4 * k + 1], m), w.y);
+      y[4 * k + 2] = sr_round<FMT>(__fmul_rn(v[4 * k + 2], m), w.z);
+      y[4 * k + 3] = sr_round<FMT>(__fmul_rn(v[4 * k + 3], m), w.w);
+    }
+  } else if (EXTRA && p.rounding == MXQ_SR4) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      y[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw4(idx0 + j * istep, p.sr_k0, p.sr_k1));
+  } else if (EXTRA && p.rounding == MXQ_SR) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       y[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw(idx0 + j * istep, p.sr_k0, p.sr_k1));
@@ -720,7 +745,7 @@ int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap
 template <bool PT>
 int dispatch(int fmt, int orient, const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc,
              const QuantParams& p, cudaStream_t st) {
-  const bool extra = !PT && (p.rounding == MXQ_SR || p.hadamard);
+  const bool extra = !PT && (p.rounding != MXQ_RNE || p.hadamard);
 #define MXQ_CASE(F, O)                                                                  \
   if (fmt == F && orient == O)                                                          \
     return extra ? launch_tiles<F, O, PT, !PT>(mx, mr, mc, p, st)                      \
@@ -773,7 +798,7 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                             uint8_t* s_col, void* stream) {
   if (!x || !valid_fmt(fmt) || !valid_orient(orient)) return MXQ_ERR_BAD_ARG;
   if (scale_mode != MXQ_SCALE_FLOOR_OCP && scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
-  if (rounding != MXQ_RNE && rounding != MXQ_SR) return MXQ_ERR_BAD_ARG;
+  if (rounding != MXQ_RNE && rounding != MXQ_SR && rounding != MXQ_SR4) return MXQ_ERR_BAD_ARG;
   if (sf_layout != MXQ_SF_CANONICAL && sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
   if ((orient & MXQ_ROW) && (!q_row || !s_row)) return MXQ_ERR_BAD_ARG;
   if ((orient & MXQ_COL) && (!q_col || !s_col)) return MXQ_ERR_BAD_ARG;

@@ -78,9 +78,14 @@ extern "C" {
  * at the format maximum, sign kept on zero.  SR: stochastic rounding with
  * r = word 0 of Philox-4x32-10(key = sr_key, counter = (i, i >> 32, 0, 0)),
  * i = r*cols + c the element's index in x; with y' = min(|y|, max) between
- * grid neighbours lo < y' < hi, round up iff r < floor((y'-lo)/(hi-lo)*2^32). */
+ * grid neighbours lo < y' < hi, round up iff r < floor((y'-lo)/(hi-lo)*2^32).
+ * SR4: the same rounding with four draws per generator call: r = word
+ * (i & 3) of Philox-4x32-10(key = sr_key, counter = (c, c >> 32, 0, 0)),
+ * c = i >> 2 (an option of this library, not of the pages: a quarter of the
+ * generator work of SR, different draws). */
 #define MXQ_RNE 0
 #define MXQ_SR  1
+#define MXQ_SR4 2
 /* Scale-factor layout.
  * CANONICAL: row-major bytes, s_row [rows][cols/32], s_col [cols][rows/32].
  * MMA: the layout the GEMM's tensor-core scale path reads ([FAF]: the
@@ -100,7 +105,7 @@ extern "C" {
  * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1.
  * orient   MXQ_ROW | MXQ_COL | MXQ_DUAL.
  * scale_mode  MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL.
- * rounding MXQ_RNE | MXQ_SR.
+ * rounding MXQ_RNE | MXQ_SR | MXQ_SR4.
  * hadamard32  non-zero: before scale selection each 32-block (along its
  *          block direction) becomes y = c * H32 * D * v in float32: D holds
  *          the 32 signs given by bit j of word 0 of
@@ -164,6 +169,17 @@ int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
 int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q,
              const uint8_t* b_s, int64_t M, int64_t N, int64_t K, int fmt,
              int sf_layout, void* c, int out_fp32, void* stream);
+
+/* ---- mixed-format block-scaled GEMM (same product; [MX] FP8 section: E4M3
+ * for precision beside E5M2 for range, e.g. an E5M2 gradient times an E4M3
+ * operand) ----------------------------------------------------------------------
+ * As mxq_gemm, with a_fmt for A and b_fmt for B: any of E4M3 / E5M2 with
+ * either, or E2M1 with E2M1.  E2M1 beside an 8-bit format returns
+ * MXQ_ERR_UNSUPPORTED. */
+int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt,
+                   const void* b_q, const uint8_t* b_s, int b_fmt,
+                   int64_t M, int64_t N, int64_t K, int sf_layout, void* c,
+                   int out_fp32, void* stream);
 
 /* ---- scale layout conversion ([FAF]) -----------------------------------------
  * Canonical scales s [rows][kb] -> MMA layout (rows % 128 == 0,

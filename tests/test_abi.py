@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_sf_to_mma",
+    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed", "mxq_sf_to_mma",
               "mxq_last_device_status", "mxq_strerror", "mxq_version"):
         assert n in names
 
@@ -59,7 +59,7 @@ def test_argument_checks_need_no_gpu(so):
     assert q(FAKE, 64, 64, 64, 9, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
     assert q(FAKE, 64, 64, 64, 0, 4, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
     assert q(FAKE, 64, 64, 64, 0, 1, 2, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
-    assert q(FAKE, 64, 64, 64, 0, 1, 0, 2, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
+    assert q(FAKE, 64, 64, 64, 0, 1, 0, 3, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
     assert q(FAKE, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 5, FAKE, FAKE, None, None, None) == -1
     # missing column outputs for DUAL
     assert q(FAKE, 64, 64, 64, 0, 3, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -1
@@ -84,6 +84,13 @@ def test_argument_checks_need_no_gpu(so):
     assert g(FAKE, FAKE, FAKE, FAKE, 100, 128, 128, 0, 1, FAKE, 0, None) == -2
     assert g(FAKE, FAKE, FAKE, FAKE, 128, 128, 128, 2, 1, FAKE, 0, None) == -2   # E2M1 needs K % 256
     assert g(ODD, FAKE, FAKE, FAKE, 128, 128, 128, 0, 1, FAKE, 0, None) == -3
+
+    mg = so.mxq_gemm_mixed
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 2, 128, 128, 256, 1, FAKE, 0, None) == -4   # E4M3 x E2M1
+    assert mg(FAKE, FAKE, 2, FAKE, FAKE, 1, 128, 128, 256, 1, FAKE, 0, None) == -4   # E2M1 x E5M2
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 5, 128, 128, 256, 1, FAKE, 0, None) == -1   # unknown format
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 100, 128, 256, 1, FAKE, 0, None) == -2
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 128, 128, 256, 0, FAKE, 0, None) == -4   # canonical scales
 
     assert so.mxq_dequantize(FAKE, FAKE, 64, 48, 0, 1, FAKE, None) == -2
     assert so.mxq_sf_to_mma(FAKE, 100, 4, FAKE, None) == -2

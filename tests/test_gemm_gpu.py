@@ -27,10 +27,10 @@ def oracle_operand(x_f64, fmt, mode=omx.FLOOR):
     return r["q_row"], r["s_row"]
 
 
-def gpu_gemm(lib, aq, as_, bq, bs, fmt, out_dtype=torch.bfloat16):
+def gpu_gemm(lib, aq, as_, bq, bs, fmt, out_dtype=torch.bfloat16, b_fmt=None):
     dev = torch.device("cuda")
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    c = lib.mx_gemm(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt, out_dtype)
+    c = lib.mx_gemm(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt, out_dtype, b_fmt=b_fmt)
     return c.float().cpu().numpy().astype(np.float64)
 
 
@@ -70,6 +70,44 @@ def test_random_gemm_gate(lib, fmt, mnk):
     got = gpu_gemm(lib, aq, as_, bq, bs, fmt)
     err = og.gate_error(got, ref)
     assert err <= TOL, (err, og.frobenius_rel(got, ref))
+
+
+MIXED = [("e4m3", "e5m2"), ("e5m2", "e4m3")]
+
+
+@pytest.mark.parametrize("fa,fb", MIXED)
+@pytest.mark.parametrize("mn", [(128, 256), (256, 512)])
+def test_mixed_formats_unit_rows_exactly(lib, fa, fb, mn):
+    """A in one 8-bit format, B (unit rows) in the other: C[:, n] is a
+    scaled copy of one dequantized A column, exact in bf16, so each
+    operand's element type in the instruction descriptor is checked."""
+    rng = np.random.default_rng(3)
+    M, N = mn
+    K = 512
+    a = rng.standard_normal((M, K)) * np.exp2(rng.integers(-6, 6, size=(M, K // 32))).repeat(32, 1)
+    aq, as_ = oracle_operand(a, fa)
+    perm = rng.permutation(K)[:N]
+    b = np.zeros((N, K))
+    b[np.arange(N), perm] = np.exp2(rng.integers(-3, 4, size=N)) * 1.5
+    bq, bs = oracle_operand(b, fb)
+    ref = og.reference(aq, as_, bq, bs, FMTS[fa], FMTS[fb])
+    got = gpu_gemm(lib, aq, as_, bq, bs, fa, b_fmt=fb)
+    assert np.array_equal(got, ref), f"max abs diff {np.max(np.abs(got - ref))}"
+
+
+@pytest.mark.parametrize("fa,fb", MIXED)
+@pytest.mark.parametrize("mnk", [(256, 512, 1024), (384, 384, 512), (512, 768, 2048)])
+def test_mixed_formats_gate(lib, fa, fb, mnk):
+    """E5M2 gradients times E4M3 weights (and the reverse) against the
+    float64 product of the dequantized operands."""
+    M, N, K = mnk
+    a = f64(inputs.gradients(M, K, seed=1) if fa == "e5m2" else inputs.activations(M, K, seed=0))
+    b = f64(inputs.gradients(N, K, seed=2) if fb == "e5m2" else inputs.weights(N, K, seed=4))
+    aq, as_ = oracle_operand(a, fa)
+    bq, bs = oracle_operand(b, fb)
+    ref = og.reference(aq, as_, bq, bs, FMTS[fa], FMTS[fb])
+    got = gpu_gemm(lib, aq, as_, bq, bs, fa, b_fmt=fb)
+    assert og.gate_error(got, ref) <= TOL, (og.gate_error(got, ref), og.frobenius_rel(got, ref))
 
 
 def test_fp32_output_and_many_tiles(lib):

@@ -21,13 +21,13 @@ pytestmark = pytest.mark.gpu
 FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2, "e2m1": F.E2M1}
 ORI = {"row": omx.ROW, "col": omx.COL, "dual": omx.DUAL}
 MODE = {"floor": omx.FLOOR, "ceil": omx.CEIL}
+ROUND = {"rne": omx.RNE, "sr": omx.SR, "sr4": omx.SR4}
 
 
 def run_both(lib, x, fmt, orient, mode, rounding="rne", had=False, sr_key=0, had_seed=7, sf="canonical"):
     dev = torch.device("cuda")
     out = lib.mx_quantize(x.to(dev), fmt, orient, mode, rounding, had, sr_key, had_seed, sf)
-    ref = omx.quantize(f64(x), FMTS[fmt], ORI[orient], MODE[mode], omx.SR if rounding == "sr" else omx.RNE,
-                       had, sr_key, had_seed)
+    ref = omx.quantize(f64(x), FMTS[fmt], ORI[orient], MODE[mode], ROUND[rounding], had, sr_key, had_seed)
     return [np_(t) for t in out], ref
 
 
@@ -137,6 +137,28 @@ def test_stochastic_rounding_and_hadamard(lib, fmt, orient):
         for key in (0, 0x123456789ABCDEF):
             got, ref = run_both(lib, g, fmt, orient, "floor", "sr", had, key, 7)
             check(got, ref, orient)
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e4m3", "e5m2"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+def test_stochastic_rounding_four_draws_per_call(lib, fmt, orient):
+    """SR4 option: row blocks take eight generator calls per block, column
+    blocks one call per element (word index & 3 of counter index >> 2)."""
+    g = inputs.heavy_gradient(160, 288, seed=9)
+    for had in (False, True):
+        for key in (0, 0x123456789ABCDEF):
+            got, ref = run_both(lib, g, fmt, orient, "floor", "sr4", had, key, 7)
+            check(got, ref, orient)
+
+
+def test_sr4_differs_from_sr_and_is_deterministic(lib):
+    g = inputs.heavy_gradient(128, 256, seed=2).cuda()
+    a = lib.mx_quantize(g, "e2m1", "row", "floor", "sr4", True, 3, 7)
+    b = lib.mx_quantize(g, "e2m1", "row", "floor", "sr4", True, 3, 7)
+    c = lib.mx_quantize(g, "e2m1", "row", "floor", "sr", True, 3, 7)
+    assert torch.equal(a[0], b[0])
+    assert not torch.equal(a[0], c[0])
+    assert torch.equal(a[1], c[1])                         # scales do not depend on the draws
 
 
 @pytest.mark.parametrize("orient", ["row", "col"])
@@ -254,6 +276,19 @@ def test_full_size_dual_sampled(lib, fmt, gen, seed, mode):
         refc = omx.quantize(xv[r0:r0 + 32], FMTS[fmt], omx.COL, MODE[mode])
         assert_bytes_equal(np_(qc)[:, r0:r0 + 32], refc["q_col"], "q_col slab")
         assert_bytes_equal(np_(sc)[:, sl:sl + 1], refc["s_col"], "s_col slab")
+
+
+def test_full_size_fp4_sr4_hadamard_sampled(lib):
+    """4096 x 14336 MXFP4, Hadamard-32 and the four-draws-per-call option."""
+    g = inputs.heavy_gradient()
+    dev = torch.device("cuda")
+    q, s, _, _ = lib.mx_quantize(g.to(dev), "e2m1", "row", "floor", "sr4", True, 0, 7, "mma")
+    gv = f64(g)
+    rows = _sample_rows(4096, 24, 4)
+    ref = omx.quantize(gv[rows], F.E2M1, omx.ROW, omx.FLOOR, omx.SR4, True, 0, 7, row_index=rows, total_cols=14336)
+    assert_bytes_equal(np_(q)[rows], ref["q_row"], "q sample")
+    s_can = omx.sf_from_mma(np_(s), 4096, 14336 // 32)
+    assert_bytes_equal(s_can[rows], ref["s_row"], "s sample")
 
 
 def test_full_size_fp4_sr_hadamard_sampled(lib):
