@@ -46,6 +46,21 @@ def reference_rows_cols(a_q, a_s, b_q, b_s, f, rows, cols, fb=None) -> np.ndarra
     return A @ B.T
 
 
+def mm_fp8_reference(a8, b8, f, scale: float, bias=None) -> np.ndarray:
+    """Per-tensor FP8 product (AstrAI fp8.py, mm_fp8: "a @ b * scale
+    (+ bias)", scale the combined dequantization scale, bias added per output
+    column): float64 C = (dec(a8) @ dec(b8)^T) * scale + bias with a8 [.., M, K]
+    and b8 [.., N, K] FP8 codes of format f (both K-contiguous; a leading batch
+    axis broadcasts like matmul) and bias [N] or None."""
+    from .formats import decode
+    A = decode(f, np.asarray(a8)).astype(np.float64)
+    B = decode(f, np.asarray(b8)).astype(np.float64)
+    C = np.matmul(A, np.swapaxes(B, -1, -2)) * float(scale)
+    if bias is not None:
+        C = C + np.asarray(bias, dtype=np.float64)
+    return C
+
+
 def ulp_bf16(x: np.ndarray) -> np.ndarray:
     """Spacing of bf16 numbers at |x| (8 significant bits; subnormal floor
     2^-133)."""

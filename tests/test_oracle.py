@@ -458,6 +458,38 @@ def test_gemm_mixed_formats_decode_each_operand():
     assert np.array_equal(sub, ref[:5, :7])
 
 
+def test_mm_fp8_reference_one_hot_rows_index_b():
+    """One-hot A rows (code for 1.0 at column perm[m]) pick B's columns:
+    C[m, n] = dec(b)[n, perm[m]] * scale + bias[n], read off by indexing
+    (no product), so a transposed operand, a missing scale or a bias added
+    per row instead of per column fails."""
+    rng = np.random.default_rng(15)
+    for f in (F.E4M3, F.E5M2):
+        M, N, K = 6, 9, 16
+        one = F.encode_rne_sat(f, np.array([1.0]))[0]
+        perm = rng.permutation(K)[:M]
+        a8 = np.zeros((M, K), dtype=np.uint8)
+        a8[np.arange(M), perm] = one
+        b8 = rng.integers(0, 0x70, (N, K), dtype=np.uint8) | (rng.integers(0, 2, (N, K), dtype=np.uint8) << 7)
+        bias = rng.standard_normal(N)
+        C = gemm.mm_fp8_reference(a8, b8, f, 0.25, bias)
+        db = F.decode(f, b8)
+        want = np.array([[db[n, perm[m]] * 0.25 + bias[n] for n in range(N)] for m in range(M)])
+        assert np.array_equal(C, want)
+
+
+def test_mm_fp8_reference_batch_broadcast():
+    """A leading batch axis on A with a shared B equals the per-batch products."""
+    rng = np.random.default_rng(16)
+    a8 = rng.integers(0, 0x70, (3, 4, 8), dtype=np.uint8)
+    b8 = rng.integers(0, 0x70, (5, 8), dtype=np.uint8)
+    C = gemm.mm_fp8_reference(a8, b8, F.E4M3, 2.0)
+    for i in range(3):
+        assert np.array_equal(C[i], gemm.mm_fp8_reference(a8[i], b8, F.E4M3, 2.0))
+    ones = np.full((2, 8), F.encode_rne_sat(F.E4M3, np.array([1.0]))[0], dtype=np.uint8)
+    assert np.array_equal(gemm.mm_fp8_reference(ones, ones, F.E4M3, 0.5), np.full((2, 2), 4.0))
+
+
 def test_gemm_pm_one_integer_sums():
     rng = np.random.default_rng(5)
     M, N, K = 32, 32, 256
