@@ -270,7 +270,33 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
                                        "unit": "TFLOP/s", "frac": round(tf / pk, 4),
                                        "peak_source": f"bf16 burst x {RATIO['e4m3']} ({peak_src})",
                                        "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"), name)}})
+    # the same MXFP8 product written as MX E4M3 codes + scales (MMA layout:
+    # the next GEMM's A operand) straight from the accumulator
+    fn = lambda: mxq.mx_gemm_mx_out(aq, as_, wq, ws, "e4m3", out_fmt="e4m3", out_sf_layout="mma")
+    n += extra_gemm_row(args, fn, timed, "mxfp8_gemm_mx_e4m3_out_8192x4096x4096", M, 4096, K, bf16, peak_src,
+                        gemm_rows)
+    # per-tensor FP8 product with scale and bias (mm_fp8): the per-tensor
+    # quantizer's E4M3 activations times E4M3 weights
+    x8 = mxq.fp8_quantize_pertensor(X["A"], X["one"], "e4m3", "row")[0]
+    w8 = mxq.fp8_quantize_pertensor(W, X["one"], "e4m3", "row")[0]
+    fn = lambda: mxq.mm_fp8(x8, w8, X["one"], trans_b=True, bias=X["bias"], fmt="e4m3")
+    n += extra_gemm_row(args, fn, timed, "fp8_pertensor_gemm_bias_8192x4096x4096", M, 4096, K, bf16, peak_src,
+                        gemm_rows)
     return n
+
+
+def extra_gemm_row(args, fn, timed, name, M, N, K, bf16, peak_src, gemm_rows):
+    for _ in range(max(3, args.warmup)):
+        fn()
+    ms = timed(fn, args.steps)
+    tf = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
+    pk = bf16 * RATIO["e4m3"]
+    gemm_rows.append({"workload": name, "ms": round(ms, 4), "tflops": round(tf, 1),
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(pk, 1),
+                                   "unit": "TFLOP/s", "frac": round(tf / pk, 4),
+                                   "peak_source": f"bf16 burst x {RATIO['e4m3']} ({peak_src})",
+                                   "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"), name)}})
+    return args.steps
 
 
 def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
@@ -406,6 +432,9 @@ def run_ours(args, rank, world):
     if args.case in ("all", "gemm"):
         X["W"] = inputs.weights(4096, 4096, seed=4).to(dev)
         X["W2"] = inputs.weights(14336, 4096, seed=5).to(dev)
+        X["A"] = A
+        X["one"] = torch.ones(1, dtype=torch.float32, device=dev)
+        X["bias"] = inputs.weights(1, 4096, seed=9).reshape(4096).to(dev)
     if args.case in ("all", "fp4"):
         X["G5"] = inputs.heavy_gradient().to(dev)
         X["B5"] = inputs.fp4_operand().to(dev)

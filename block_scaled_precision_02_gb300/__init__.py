@@ -59,13 +59,16 @@ def load() -> ctypes.CDLL:
     L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
     L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
     L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
+    L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp]
+    L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
     L.mxq_last_device_status.argtypes = [vp]
     L.mxq_strerror.argtypes = [i32]
     L.mxq_strerror.restype = ctypes.c_char_p
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
-    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed", "mxq_sf_to_mma",
+    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed",
+                 "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32
     _lib = L
@@ -210,6 +213,75 @@ def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.
         rc = load().mxq_gemm_mixed(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, _SF[sf_layout],
                                    _ptr(c), int(out_dtype == torch.float32), _stream(a_q.device))
     _check(rc, "mxq_gemm")
+    return c
+
+
+def mx_gemm_mx_out(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.Tensor, fmt="e4m3",
+                   b_fmt=None, out_fmt="e4m3", out_scale_mode="floor", out_sf_layout="canonical",
+                   K: Optional[int] = None):
+    """A * B^T as mx_gemm, written as MX codes and scales of 1x32 row blocks
+    (out_fmt, out_scale_mode, out_sf_layout) straight from the accumulator.
+    Returns (codes uint8 [M][N], scales uint8 [M][N/32] or the MMA-layout
+    bytes)."""
+    f = _FMT[fmt]
+    fb = f if b_fmt is None else _FMT[b_fmt]
+    M = a_q.shape[0]
+    N = b_q.shape[0]
+    if K is None:
+        K = a_q.shape[1] * (2 if f == E2M1 else 1)
+    dev = a_q.device
+    cq = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    cs = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
+    rc = load().mxq_gemm_mx_out(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, SF_MMA, _FMT[out_fmt],
+                                _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _stream(dev))
+    _check(rc, "mxq_gemm_mx_out")
+    return cq, cs
+
+
+def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool = False, trans_b: bool = False,
+           bias: Optional[torch.Tensor] = None, fmt: Optional[str] = None) -> torch.Tensor:
+    """Per-tensor FP8 GEMM ``op(a) @ op(b) * scale (+ bias)`` (AstrAI fp8.py
+    mm_fp8), bf16 result.  ``a``/``b`` hold FP8 codes (uint8 or a torch
+    float8 dtype, which also gives the format), 2-D or 3-D (a batch axis
+    broadcasts); op transposes the last two axes when the flag is set.
+    Views fold into the layout at zero copy as long as op(a) has K-contiguous
+    rows and op(b) K-contiguous columns (op(b) = w.t() for a row-major [N][K]
+    w); other layouts raise ValueError.  ``scale`` is a 1-element device
+    float32 tensor, ``bias`` a bf16 [N] vector."""
+    if fmt is None:
+        names = {getattr(torch, "float8_e4m3fn", None): "e4m3", getattr(torch, "float8_e5m2", None): "e5m2"}
+        fmt = names.get(a.dtype, "e4m3")
+    f = _FMT[fmt]
+    A = a.transpose(-1, -2) if trans_a else a
+    B = b.transpose(-1, -2) if trans_b else b
+    if A.dim() not in (2, 3) or B.dim() not in (2, 3):
+        raise ValueError("mm_fp8 takes 2-D or 3-D operands")
+    M, K = A.shape[-2], A.shape[-1]
+    if B.shape[-2] != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {B.shape[-2]}")
+    N = B.shape[-1]
+    if A.stride(-1) != 1 or A.stride(-2) != K:
+        raise ValueError("op(a) must have K-contiguous rows (row-major [M][K])")
+    if B.stride(-2) != 1 or B.stride(-1) != K:
+        raise ValueError("op(b) must be the transposed view of a row-major [N][K] operand")
+    ba = A.shape[0] if A.dim() == 3 else 1
+    bb = B.shape[0] if B.dim() == 3 else 1
+    if ba > 1 and bb > 1 and ba != bb:
+        raise ValueError(f"batch sizes differ: {ba} vs {bb}")
+    batch = max(ba, bb)
+    if A.dim() == 3 and ba > 1 and A.stride(0) != M * K:
+        raise ValueError("a's batch entries must be contiguous")
+    if B.dim() == 3 and bb > 1 and B.stride(0) != N * K:
+        raise ValueError("b's batch entries must be contiguous")
+    if scale.dtype != torch.float32 or scale.numel() != 1 or not scale.is_cuda:
+        raise ValueError("scale must be a 1-element float32 CUDA tensor")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous bf16 vector of length n")
+    shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
+    c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
+    rc = load().mxq_mm_fp8(_ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), f, _ptr(scale),
+                           _ptr(bias), _ptr(c), _stream(a.device))
+    _check(rc, "mxq_mm_fp8")
     return c
 
 

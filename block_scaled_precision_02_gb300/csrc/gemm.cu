@@ -1,11 +1,15 @@
-// Block-scaled (MX) GEMM on the sm_103a tensor cores:
-//   C[m][n] = sum_k dec(a[m][k]) 2^(sa[m][k/32]-127) dec(b[n][k]) 2^(sb[n][k/32]-127)
-// with float32 accumulation in tensor memory and a bf16 (or float32) output.
-//
-// Source: "UE8M0 FP8 / MXFP8 explainer", section 1 -- tensor cores consume the
-// UE8M0 scale X and the element codes q_i of both operands, block by block,
-// and accumulate in FP32; gap section 2 -- the blocks must run along the
-// contiguous reduction dimension (both operands K-contiguous, C = A * B^T).
+// GEMMs on the sm_103a tensor cores, C = A * B^T with both operands
+// K-contiguous and float32 accumulation in tensor memory:
+//  * block-scaled (MX):
+//      C[m][n] = sum_k dec(a[m][k]) 2^(sa[m][k/32]-127) dec(b[n][k]) 2^(sb[n][k/32]-127)
+//    Source: "UE8M0 FP8 / MXFP8 explainer", section 1 -- tensor cores consume
+//    the UE8M0 scale X and the element codes q_i of both operands, block by
+//    block, and accumulate in FP32; gap section 2 -- the blocks must run
+//    along the contiguous reduction dimension.  Output bf16 or float32, or
+//    (format-aware fusion: the producer writes its consumer's format) MX
+//    codes and scales of 1 x 32 row blocks quantized from the accumulator.
+//  * per-tensor FP8 (AstrAI fp8.py, mm_fp8): C = (A * B^T) * scale + bias,
+//    bf16 out, optionally batched.
 //
 // Two kernels share the warp roles below.
 //  * CTA pair (M and N multiples of 256): clusters of two CTAs on two SMs
@@ -22,16 +26,17 @@
 //                512-byte scale chunks (the quantizer already wrote them in
 //                the tensor-core layout), into a ring of stages.
 //  * warp 1      allocates tensor memory; one thread (of the pair's first
-//                CTA) issues 4 block-scaled tcgen05.mma per stage (E4M3/E5M2:
+//                CTA) issues 4 tcgen05.mma per stage (E4M3/E5M2 block-scaled:
 //                kind::mxf8f6f4, scale_vec::1X, K = 32; E2M1: kind::mxf4,
-//                scale_vec::2X, K = 64), then tcgen05.commit to free the
-//                stage (in both CTAs of a pair).  The single-CTA kernel
-//                issues the tcgen05.cp of the scale chunks into tensor memory
-//                from the same thread; the pair kernel leaves them to warp 6,
-//                which runs ahead of the MMAs.
+//                scale_vec::2X, K = 64; per-tensor FP8: kind::f8f6f4), then
+//                tcgen05.commit to free the stage (in both CTAs of a pair).
+//                The single-CTA kernel issues the tcgen05.cp of the scale
+//                chunks into tensor memory from the same thread; the pair
+//                kernel leaves them to warp 6, which runs ahead of the MMAs.
 //  * warps 2..5  epilogue: tcgen05.ld of this CTA's 128 x N float32
 //                accumulator rows (each thread owns one row), conversion,
-//                and TMA stores through two 64-byte-swizzled staging buffers.
+//                and stores (TMA through two 64-byte-swizzled staging
+//                buffers; the MX output is stored directly).
 // Every wait is bounded (1 s); on expiry the status word records
 // MXQ_ERR_TIMEOUT, all roles wind down, in-flight copies are awaited (with a
 // limit) and tensor memory is released.
@@ -50,18 +55,44 @@ constexpr int EPI_WARP0 = 2;
 constexpr int PAIR_THREADS = 224;     // pair kernel: the roles above plus warp 6 (scale copies)
 constexpr int STG_BYTES = BM * 64;       // one staging buffer: 128 rows x 64 B
 
+// Operand kinds (a template parameter of both kernels).
+constexpr int KIND_MXF8 = 0;   // block-scaled E4M3 / E5M2: kind::mxf8f6f4, scale_vec::1X
+constexpr int KIND_MXF4 = 1;   // block-scaled E2M1 (packed): kind::mxf4, scale_vec::2X
+constexpr int KIND_F8 = 2;     // per-tensor E4M3 / E5M2: kind::f8f6f4, no block scales
+
+// Epilogue modes.
+constexpr int EPI_BF16 = 0;    // bf16 (RNE); per-tensor kind: RN32(RN32(acc * scale) + bias) first
+constexpr int EPI_FP32 = 1;    // float32 accumulator as is
+constexpr int EPI_MX = 2;      // MX codes + UE8M0 scales of 1 x 32 row blocks
+
 struct Params {
   const uint8_t* a_s;
   const uint8_t* b_s;
   int M, N, K;
-  int tiles_m, tiles_n, ntiles;
+  int tiles_m, tiles_n, ntiles;   // tiles_m x tiles_n per product; ntiles over all batches
   int kblocks;        // K steps of BKB bytes
   int kb4;            // 512-byte scale chunks per 128 rows (K / 128)
-  int out_fp32;
+  int a_batched, b_batched;       // 1: operand rows advance by M (N) per batch; 0: shared
+  int epi;
+  const float* alpha;             // per-tensor kind: combined dequantization scale (device scalar)
+  const __nv_bfloat16* bias;      // per-tensor kind: bias[N] or nullptr
+  uint8_t* cq;                    // EPI_MX: codes [M][N]
+  uint8_t* cs;                    // EPI_MX: scales, canonical [M][N/32] or the MMA layout
+  int mx_fmt, mx_ceil, mx_sf_mma;
   int* status;
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
+
+// Batch, first row and first column of output tile `tile` (tm x tn tiles).
+struct TilePos {
+  int b, m0, n0;
+};
+__device__ __forceinline__ TilePos tile_pos(const Params& p, int tile, int tm, int tn) {
+  const int per = p.tiles_m * p.tiles_n;
+  const int b = tile / per, r = tile - b * per;
+  return {b, (r / p.tiles_n) * tm, (r % p.tiles_n) * tn};
+}
 
 // ---------------------------------------------------------------- tcgen05 wrappers
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -84,20 +115,26 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-template <bool FP4>
+template <int KIND>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t acc) {
-  if constexpr (FP4) {
+  if constexpr (KIND == KIND_MXF4) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
         : "memory");
-  } else {
+  } else if constexpr (KIND == KIND_MXF8) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
   }
 }
@@ -140,20 +177,26 @@ __device__ __forceinline__ void tc_commit_pair_self(uint32_t bar) {
 __device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
-template <bool FP4>
+template <int KIND>
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
                                             uint32_t sfb, uint32_t acc) {
-  if constexpr (FP4) {
+  if constexpr (KIND == KIND_MXF4) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
         : "memory");
-  } else {
+  } else if constexpr (KIND == KIND_MXF8) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
   }
 }
@@ -182,33 +225,86 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_type, uint32_t b_ty
          (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
 }
 
+// Instruction descriptor of the unscaled kind::f8f6f4 MMA: float32
+// accumulator (bits 4-5 = 1), A / B element types at bits 7-9 / 10-12,
+// K-major operands, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc_f8(uint32_t a_type, uint32_t b_type, int n, int m) {
+  return (1u << 4) | (a_type << 7) | (b_type << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+template <int KIND>
+__device__ __forceinline__ uint32_t mma_idesc(const Params& p, int n, int m, int kk) {
+  if constexpr (KIND == KIND_F8) return instr_desc_f8(p.a_type, p.b_type, n, m);
+  else return instr_desc(p.a_type, p.b_type, n, m, KIND == KIND_MXF4 ? (kk & 1) * 2 : kk);
+}
+
+// Four float32 -> four FP8 codes (RNE, saturating) in the given format.
+__device__ __forceinline__ uint32_t fp8x4_rt(int fmt, float a, float b, float c, float d) {
+  return fmt == MXQ_E4M3 ? cvt_fp8x4<MXQ_E4M3>(a, b, c, d) : cvt_fp8x4<MXQ_E5M2>(a, b, c, d);
+}
+
+// MX quantization of one 32-value row block of the accumulator: the scale
+// rule of the quantizer (floor or ceil on the block amax's exponent and
+// mantissa bits), then codes = RNE-saturating FP8 of v * 2^-e (exact
+// product).  A block holding NaN or Inf gets scale 0xFF and zero codes.
+__device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt, int ceil_mode,
+                                               uint32_t* codes /* 8 words */) {
+  uint32_t ab = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ab = max(ab, v[j] & 0x7FFFFFFFu);
+  const bool bad = ab >= 0x7F800000u;
+  const int e = bad ? 0 : (fmt == MXQ_E4M3 ? scale_exp<MXQ_E4M3>(ab, ceil_mode) : scale_exp<MXQ_E5M2>(ab, ceil_mode));
+  const float m = exp2_neg(e);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t x = fp8x4_rt(fmt, __fmul_rn(__uint_as_float(v[4 * k]), m), __fmul_rn(__uint_as_float(v[4 * k + 1]), m),
+                                __fmul_rn(__uint_as_float(v[4 * k + 2]), m), __fmul_rn(__uint_as_float(v[4 * k + 3]), m));
+    codes[k] = bad ? 0u : x;
+  }
+  return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+}
+
 // Epilogue of one output tile: drain this CTA's 128 x BN float32
 // accumulator (tensor-memory lanes 0..127, columns 0..BN-1; the thread of
 // lane quarter q and lane `lane` owns row 32 q + lane), call release() once
-// it has been read completely, and store it to C[m0 .., n0 ..] through two
-// 64-byte-swizzled staging buffers (TMA stores issued by `leader`).  All 128
-// epilogue threads take part (named barrier 1).
-template <int BN, typename Release>
-__device__ __forceinline__ void store_tile(uint32_t tmem, int q, int lane, bool leader, int& buf, uint8_t* sOut,
-                                           const CUtensorMap* map_c, int m0, int n0, int out_fp32, Release release) {
+// it has been read completely, and store it to C[m0 .., n0 ..] (rows of the
+// whole batched output) in the mode p.epi.  bf16 / float32 go through two
+// 64-byte-swizzled staging buffers and TMA stores issued by `leader`; all
+// 128 epilogue threads take part (named barrier 1).
+template <int BN, bool PER_TENSOR, typename Release>
+__device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_t tmem, int q, int lane, bool leader,
+                                           int& buf, uint8_t* sOut, const CUtensorMap* map_c, int m0, int n0,
+                                           Release release) {
   const int row = q * 32 + lane;
-  if (!out_fp32) {
-    // bf16: drain the whole accumulator row into registers first, so the
-    // MMA warp can start the next tile while this one is written out
-    // (two 32-column loads in flight per wait)
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  if (p.epi == EPI_BF16) {
+    // drain the whole accumulator row into registers first, so the MMA warp
+    // can start the next tile while this one is written out (two 32-column
+    // loads in flight per wait)
     uint32_t pk[BN / 2];
 #pragma unroll
     for (int c = 0; c < BN / 32; c += 2) {
       uint32_t v[2][32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v[0]);
-      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + (c + 1) * 32, v[1]);
+      tmem_ld32(lane_addr + c * 32, v[0]);
+      tmem_ld32(lane_addr + (c + 1) * 32, v[1]);
       tmem_ld_wait();
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const __nv_bfloat162 b2 =
-              __floats2bfloat162_rn(__uint_as_float(v[h][2 * j]), __uint_as_float(v[h][2 * j + 1]));
+          float x0 = __uint_as_float(v[h][2 * j]), x1 = __uint_as_float(v[h][2 * j + 1]);
+          if constexpr (PER_TENSOR) {
+            x0 = __fmul_rn(x0, alpha);
+            x1 = __fmul_rn(x1, alpha);
+            if (p.bias) {
+              const __nv_bfloat162 bb =
+                  *reinterpret_cast<const __nv_bfloat162*>(p.bias + n0 + (c + h) * 32 + 2 * j);
+              x0 = __fadd_rn(x0, __low2float(bb));
+              x1 = __fadd_rn(x1, __high2float(bb));
+            }
+          }
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
           pk[(c + h) * 16 + j] = *reinterpret_cast<const uint32_t*>(&b2);
         }
     }
@@ -236,10 +332,49 @@ __device__ __forceinline__ void store_tile(uint32_t tmem, int q, int lane, bool 
     }
     return;
   }
+  if (p.epi == EPI_MX) {
+    // each 32-column chunk of a row is one MX block: codes and the scale
+    // byte are formed from the registers, then stored straight to memory
+    uint32_t codes[BN / 4];
+    uint32_t sc[BN / 128];
+#pragma unroll
+    for (int g = 0; g < BN / 128; ++g) sc[g] = 0;
+#pragma unroll
+    for (int c = 0; c < BN / 32; c += 2) {
+      uint32_t v[2][32];
+      tmem_ld32(lane_addr + c * 32, v[0]);
+      tmem_ld32(lane_addr + (c + 1) * 32, v[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t s8 = mx_block32(v[h], p.mx_fmt, p.mx_ceil, &codes[(c + h) * 8]);
+        sc[(c + h) >> 2] |= s8 << (8 * ((c + h) & 3));
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    release();
+    const size_t rg = static_cast<size_t>(m0 + row);
+    uint4* dst = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0);
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) dst[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
+    const int kb = p.N / 32;                                     // scale columns
+#pragma unroll
+    for (int g = 0; g < BN / 128; ++g) {
+      const int j0 = n0 / 32 + 4 * g;                            // first scale column of this word
+      size_t off;
+      if (p.mx_sf_mma)                                           // chunk (rg/128, j0/4), row rg%32, word (rg/32)%4
+        off = ((rg / 128) * static_cast<size_t>(kb / 4) + j0 / 4) * 512 + (rg % 32) * 16 + ((rg / 32) % 4) * 4;
+      else
+        off = rg * static_cast<size_t>(kb) + j0;
+      *reinterpret_cast<uint32_t*>(p.cs + off) = sc[g];
+    }
+    return;
+  }
   // float32 output: chunk by chunk
   for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t v[32];
-    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+    tmem_ld32(lane_addr + c0, v);
     tmem_ld_wait();
     if (c0 + 32 == BN) {                                         // accumulator fully read
       tc_fence_before();
@@ -267,12 +402,14 @@ __device__ __forceinline__ void store_tile(uint32_t tmem, int q, int lane, bool 
   }
 }
 
-template <bool FP4_, int BN>
+template <int KIND_, int BN>
 struct Cfg {
-  static constexpr bool FP4 = FP4_;
+  static constexpr int KIND = KIND_;
+  static constexpr bool FP4 = KIND == KIND_MXF4;
+  static constexpr bool SCALED = KIND != KIND_F8;
   static constexpr int A_BYTES = BM * BKB;
   static constexpr int B_BYTES = BN * BKB;
-  static constexpr int SF_CHUNKS = FP4 ? 2 : 1;         // 512-B chunks per 128 rows per stage
+  static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
   static constexpr int SFA_BYTES = 512 * SF_CHUNKS;
   static constexpr int SFB_BYTES = 512 * SF_CHUNKS * (BN / 128);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -288,11 +425,11 @@ struct Cfg {
   static constexpr int SMEM = STAGES * (STAGE_BYTES + SFA_BYTES + SFB_BYTES) + 2 * STG_BYTES + 256 + 1024;
 };
 
-template <bool FP4, int BN>
+template <int KIND, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = Cfg<FP4, BN>;
+  using C = Cfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                                          // STAGES x A_BYTES
@@ -325,7 +462,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     fence_mbar_init();
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
-    prefetch_tensormap(&map_c);
+    if (p.epi != EPI_MX) prefetch_tensormap(&map_c);
   }
   if (warp == 1) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
   tc_fence_before();
@@ -341,21 +478,25 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (lane == 0) {
       int u = 0;                                               // stage use counter
       for (int tile = blockIdx.x; tile < p.ntiles && !*abort_flag; tile += gridDim.x) {
-        const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
-        const uint8_t* sfa_src = p.a_s + (static_cast<size_t>(m0 / 128) * p.kb4) * 512;
+        const TilePos tp = tile_pos(p, tile, BM, BN);
+        const int ar = tp.b * (p.a_batched ? p.M : 0) + tp.m0;   // operand rows
+        const int br = tp.b * (p.b_batched ? p.N : 0) + tp.n0;
         for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
           const int s = u % STAGES;
           if (!mbar_wait(smem_u32(&empty[s]), ((u / STAGES) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, C::TX_BYTES);
-          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, m0);
-          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, n0);
-          bulk_load_1d(smem_u32(sSFA + s * C::SFA_BYTES), sfa_src + kb * C::SFA_BYTES, C::SFA_BYTES, fb);
+          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
+          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
+          if constexpr (C::SCALED) {
+            const uint8_t* sfa_src = p.a_s + (static_cast<size_t>(tp.m0 / 128) * p.kb4) * 512;
+            bulk_load_1d(smem_u32(sSFA + s * C::SFA_BYTES), sfa_src + kb * C::SFA_BYTES, C::SFA_BYTES, fb);
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
-            const uint8_t* src = p.b_s + (static_cast<size_t>(n0 / 128 + h) * p.kb4) * 512 + kb * C::SFA_BYTES;
-            bulk_load_1d(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES), src, C::SFA_BYTES, fb);
+            for (int h = 0; h < BN / 128; ++h) {
+              const uint8_t* src = p.b_s + (static_cast<size_t>(tp.n0 / 128 + h) * p.kb4) * 512 + kb * C::SFA_BYTES;
+              bulk_load_1d(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES), src, C::SFA_BYTES, fb);
+            }
           }
         }
       }
@@ -376,7 +517,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
       uint32_t idesc[4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(p.a_type, p.b_type, BN, BM, C::FP4 ? (kk & 1) * 2 : kk);
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = mma_idesc<KIND>(p, BN, BM, kk);
       int u = 0, t = 0;
       for (int tile = blockIdx.x; tile < p.ntiles && !*abort_flag; tile += gridDim.x, ++t) {
         if (!mbar_wait(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
@@ -388,15 +529,18 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           tc_fence_after();
           const uint32_t sfa_t = tmem_sf + s * C::SF_COLS_STAGE;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          // scale chunks -> tensor memory (each 512-B chunk: 32 lanes x 16 B, x4 lane groups)
-#pragma unroll
-          for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_cp_sf(sfa_t + 4 * c, sfa_desc0 + ((s * C::SFA_BYTES + c * 512) >> 4));
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h)
+          if constexpr (C::SCALED) {
+            // scale chunks -> tensor memory (each 512-B chunk: 32 lanes x 16 B, x4 lane groups)
 #pragma unroll
             for (int c = 0; c < C::SF_CHUNKS; ++c)
-              tc_cp_sf(sfb_t + 4 * (BN / 128) * c + 4 * h, sfb_desc0 + ((s * C::SFB_BYTES + h * C::SFA_BYTES + c * 512) >> 4));
+              tc_cp_sf(sfa_t + 4 * c, sfa_desc0 + ((s * C::SFA_BYTES + c * 512) >> 4));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+#pragma unroll
+              for (int c = 0; c < C::SF_CHUNKS; ++c)
+                tc_cp_sf(sfb_t + 4 * (BN / 128) * c + 4 * h,
+                         sfb_desc0 + ((s * C::SFB_BYTES + h * C::SFA_BYTES + c * 512) >> 4));
+          }
           const uint64_t ad = a_desc0 + ((s * C::A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + ((s * C::B_BYTES) >> 4);
 #pragma unroll
@@ -406,7 +550,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             // the BN rows of B's chunk sit in BN / 32 consecutive columns.
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 4 * (BN / 128) * (kk >> 1) : sfb_t;
-            tc_mma<C::FP4>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma<KIND>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit(smem_u32(&empty[s]));                       // stage free when these MMAs finish
         }
@@ -420,17 +564,19 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                                      // tensor-memory lane quarter
     const bool leader = (warp == EPI_WARP0 && lane == 0);
+    const float alpha = (C::KIND == KIND_F8 && p.alpha) ? *p.alpha : 1.0f;
     int t = 0, buf = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++t) {
-      const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
+      const TilePos tp = tile_pos(p, tile, BM, BN);
       // the four warps decide together, so none is left alone at a named barrier
       if (!mbar_wait(smem_u32(acc_full), t & 1, p.status)) *epi_fail = 1;
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<BN>(tmem, q, lane, leader, buf, sOut, &map_c, m0, n0, p.out_fp32, [&] {
-        if (lane == 0) mbar_arrive(smem_u32(acc_empty));
-      });
+      store_tile<BN, C::KIND == KIND_F8>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, tp.b * p.M + tp.m0,
+                                         tp.n0, [&] {
+                                           if (lane == 0) mbar_arrive(smem_u32(acc_empty));
+                                         });
     }
     if (leader) bulk_wait_all();
   }
@@ -450,14 +596,16 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // accumulator-empty barrier (all 8 epilogue warps arrive) and issues the
 // tensor-core work (scale copies from warp 6, MMAs from warp 1); its MMA
 // commits arrive on the "empty" and accumulator-full barriers of both CTAs.
-template <bool FP4_>
+template <int KIND_>
 struct PairCfg {
-  static constexpr bool FP4 = FP4_;
+  static constexpr int KIND = KIND_;
+  static constexpr bool FP4 = KIND == KIND_MXF4;
+  static constexpr bool SCALED = KIND != KIND_F8;
   static constexpr int BN = 256;                        // columns per tile (both CTAs)
   static constexpr int STAGES = FP4 ? 5 : 6;
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
-  static constexpr int SF_CHUNKS = FP4 ? 2 : 1;         // 512-B chunks per 128 rows per stage
+  static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
   static constexpr int SFA_BYTES = 512 * SF_CHUNKS;
   static constexpr int SFB_BYTES = 2 * SFA_BYTES;       // both 128-row halves of B
   static constexpr int TX_CTA = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -470,12 +618,12 @@ struct PairCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <bool FP4>
+template <int KIND>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
                     const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = PairCfg<FP4>;
+  using C = PairCfg<KIND>;
   constexpr int STAGES_P = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -515,9 +663,11 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     fence_mbar_init();
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
-    prefetch_tensormap(&map_sfa);
-    prefetch_tensormap(&map_sfb);
-    prefetch_tensormap(&map_c);
+    if (C::SCALED) {
+      prefetch_tensormap(&map_sfa);
+      prefetch_tensormap(&map_sfb);
+    }
+    if (p.epi != EPI_MX) prefetch_tensormap(&map_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
   tc_fence_before();
@@ -533,22 +683,26 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     if (lane == 0) {
       int u = 0;                                               // stage use counter
       for (int tile = pair; tile < p.ntiles && !*abort_flag; tile += npairs) {
-        const int m0 = (tile / p.tiles_n) * 256 + static_cast<int>(rank) * BM;
-        const int nt = (tile % p.tiles_n) * 256;
+        const TilePos tp = tile_pos(p, tile, 256, 256);
+        const int m0 = tp.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the product
+        const int ar = tp.b * (p.a_batched ? p.M : 0) + m0;
+        const int br = tp.b * (p.b_batched ? p.N : 0) + tp.n0 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
           const int s = u % STAGES_P;
           if (!mbar_wait_suspend(smem_u32(&empty[s]), ((u / STAGES_P) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (rank == 0 && blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = cluster_map(smem_u32(&full[s]), 0);
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::TX_CTA);
-          tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, m0);
-          tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, nt + static_cast<int>(rank) * 128);
-          // scale maps: one 512-B chunk per row, chunk (rb, kc) at row rb * kb4 + kc
-          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &map_sfa, fb, 0, (m0 / 128) * p.kb4 + kb * C::SF_CHUNKS);
+          tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
+          tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
+          if constexpr (C::SCALED) {
+            // scale maps: one 512-B chunk per row, chunk (rb, kc) at row rb * kb4 + kc
+            tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &map_sfa, fb, 0, (m0 / 128) * p.kb4 + kb * C::SF_CHUNKS);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES), &map_sfb, fb, 0,
-                             (nt / 128 + h) * p.kb4 + kb * C::SF_CHUNKS);
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + h * C::SFA_BYTES), &map_sfb, fb, 0,
+                               (tp.n0 / 128 + h) * p.kb4 + kb * C::SF_CHUNKS);
+          }
         }
       }
       // rank 0: make sure no copy of either CTA is still landing when the pair ends
@@ -564,21 +718,23 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // ------------------------------------------------------------ MMA issuer (rank 0)
     // The tensor pipe takes only a few instructions ahead, so every cycle
     // this thread spends elsewhere can idle it: it waits for a slot's scales
-    // (copied by warp 6, which runs ahead) and issues the four MMAs only.
+    // (copied by warp 6, which runs ahead) -- or, unscaled, for the slot's
+    // operands -- and issues the four MMAs only.
     if (lane == 0 && rank == 0) {
       const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
       uint32_t idesc[4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) idesc[kk] = instr_desc(p.a_type, p.b_type, C::BN, 2 * BM, C::FP4 ? (kk & 1) * 2 : kk);
+      for (int kk = 0; kk < 4; ++kk) idesc[kk] = mma_idesc<KIND>(p, C::BN, 2 * BM, kk);
       const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
+      uint64_t* ready = C::SCALED ? sf_full : full;
       bool ok = true;
       int s = 0, ph = 0;
       for (int t = 0; t < my_tiles && ok && !*abort_flag; ++t) {
         if (!mbar_wait_suspend(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait_suspend(smem_u32(&sf_full[s]), ph, p.status)) { ok = false; break; }
+          if (!mbar_wait_suspend(smem_u32(&ready[s]), ph, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfa_t = tmem_sf + s * C::SF_COLS_STAGE;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
@@ -588,7 +744,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 8 * (kk >> 1) : sfb_t;
-            tc_mma_pair<C::FP4>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma_pair<KIND>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit_pair_both(smem_u32(&empty[s]));            // stage free in both CTAs
           if (++s == STAGES_P) { s = 0; ph ^= 1; }
@@ -607,7 +763,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // then a commit that tells the MMA issuer they have landed.  A slot is
     // rewritten only after its stage was refilled, i.e. after the MMAs that
     // read its previous scales completed.
-    if (lane == 0 && rank == 0) {
+    if (C::SCALED && lane == 0 && rank == 0) {
       const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 0, 128, 0);
       const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
       const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
@@ -637,15 +793,16 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const int q = warp & 3;
     const bool leader = (warp == EPI_WARP0 && lane == 0);
     const uint32_t acc_empty_r0 = cluster_map(smem_u32(acc_empty), 0);
+    const float alpha = (C::KIND == KIND_F8 && p.alpha) ? *p.alpha : 1.0f;
     int t = 0, buf = 0;
     for (int tile = pair; tile < p.ntiles; tile += npairs, ++t) {
-      const int m0 = (tile / p.tiles_n) * 256 + static_cast<int>(rank) * BM;
-      const int n0 = (tile % p.tiles_n) * 256;
+      const TilePos tp = tile_pos(p, tile, 256, 256);
+      const int m0 = tp.b * p.M + tp.m0 + static_cast<int>(rank) * BM;   // rows of the batched output
       if (!mbar_wait_suspend(smem_u32(acc_full), t & 1, p.status)) *epi_fail = 1;
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<C::BN>(tmem, q, lane, leader, buf, sOut, &map_c, m0, n0, p.out_fp32, [&] {
+      store_tile<C::BN, C::KIND == KIND_F8>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, m0, tp.n0, [&] {
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(acc_empty));
           else mbar_arrive_remote(acc_empty_r0);
@@ -672,42 +829,84 @@ using namespace mxq_host;
 
 namespace {
 
-template <bool FP4, int BN>
-int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-           int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, cudaStream_t st) {
-  using namespace mxq::gemm;
-  using Cf = Cfg<FP4, BN>;
-  const int64_t kbytes = Cf::FP4 ? K / 2 : K;
-  CUtensorMap ma, mb, mc;
-  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, kbytes, M, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
-  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, kbytes, N, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
-  if (out_fp32) {
-    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M, N * 4, 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
-      return MXQ_ERR_CUDA;
-  } else {
-    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, N, M, N * 2, 32, BM, CU_TENSOR_MAP_SWIZZLE_64B))
-      return MXQ_ERR_CUDA;
-  }
+using mxq::gemm::Params;
+
+// One product as the entry points describe it.
+struct GemmArgs {
+  const void* a_q;
+  const uint8_t* a_s;
+  const void* b_q;
+  const uint8_t* b_s;
+  int64_t batch, M, N, K;
+  int a_batched, b_batched;
+  uint32_t a_type, b_type;
+  int epi;
+  void* c;                        // EPI_BF16 / EPI_FP32 output [batch * M][N]
+  const float* alpha;
+  const void* bias;
+  uint8_t* cq;
+  uint8_t* cs;
+  int mx_fmt, mx_ceil, mx_sf_mma;
+};
+
+Params make_params(const GemmArgs& g, int tm, int tn, int64_t kbytes) {
   Params p{};
-  p.a_s = a_s;
-  p.b_s = b_s;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  p.tiles_m = static_cast<int>(M / BM);
-  p.tiles_n = static_cast<int>(N / BN);
-  p.ntiles = p.tiles_m * p.tiles_n;
-  p.kblocks = static_cast<int>(kbytes / BKB);
-  p.kb4 = static_cast<int>(K / 128);
-  p.out_fp32 = out_fp32;
+  p.a_s = g.a_s;
+  p.b_s = g.b_s;
+  p.M = static_cast<int>(g.M);
+  p.N = static_cast<int>(g.N);
+  p.K = static_cast<int>(g.K);
+  p.tiles_m = static_cast<int>(g.M / tm);
+  p.tiles_n = static_cast<int>(g.N / tn);
+  p.ntiles = static_cast<int>(g.batch) * p.tiles_m * p.tiles_n;
+  p.kblocks = static_cast<int>(kbytes / mxq::gemm::BKB);
+  p.kb4 = static_cast<int>(g.K / 128);
+  p.a_batched = g.a_batched;
+  p.b_batched = g.b_batched;
+  p.epi = g.epi;
+  p.alpha = g.alpha;
+  p.bias = static_cast<const __nv_bfloat16*>(g.bias);
+  p.cq = g.cq;
+  p.cs = g.cs;
+  p.mx_fmt = g.mx_fmt;
+  p.mx_ceil = g.mx_ceil;
+  p.mx_sf_mma = g.mx_sf_mma;
   p.status = status_ptr();
-  p.a_type = a_type;
-  p.b_type = b_type;
+  p.a_type = g.a_type;
+  p.b_type = g.b_type;
   p.stall_u = take_test_stall(2) ? 0 : -1;
+  return p;
+}
+
+// The output map: bf16 [rows][N] boxes of 32 columns, or float32 boxes of 16,
+// both 128 rows with the 64-byte swizzle; the MX output needs none.
+bool encode_c(CUtensorMap* mc, const GemmArgs& g) {
+  *mc = CUtensorMap{};
+  if (g.epi == mxq::gemm::EPI_MX) return true;
+  const uint64_t rows = static_cast<uint64_t>(g.batch * g.M);
+  if (g.epi == mxq::gemm::EPI_FP32)
+    return encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.c, g.N, rows, g.N * 4, 16, mxq::gemm::BM,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+  return encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.c, g.N, rows, g.N * 2, 32, mxq::gemm::BM,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+template <int KIND, int BN>
+int launch(const GemmArgs& g, cudaStream_t st) {
+  using namespace mxq::gemm;
+  using Cf = Cfg<KIND, BN>;
+  const int64_t kbytes = Cf::FP4 ? g.K / 2 : g.K;
+  CUtensorMap ma, mb, mc;
+  const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
+  const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
+  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_q, kbytes, arows, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXQ_ERR_CUDA;
+  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_q, kbytes, brows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXQ_ERR_CUDA;
+  if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
+  Params p = make_params(g, BM, BN, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
-  auto kern = mx_gemm_kernel<FP4, BN>;
+  auto kern = mx_gemm_kernel<KIND, BN>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -722,14 +921,14 @@ int launch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* 
 
 // Co-resident clusters of two for the pair kernel (cached per device and
 // kernel); 0 if the device cannot hold one.
-template <bool FP4>
+template <int KIND>
 int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
               int smem) {
   static int cache[64] = {};
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (cache[dev & 63]) return cache[dev & 63];
+  if (cache[dev & 63]) return cache[dev & 63] > 0 ? cache[dev & 63] : 0;
   if (!attr_set[dev & 63]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     attr_set[dev & 63] = true;
@@ -754,87 +953,96 @@ int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, C
   return n > 0 ? n : 0;
 }
 
-template <bool FP4>
-int launch_pair(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-                int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, int pairs, cudaStream_t st) {
+template <int KIND>
+int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   using namespace mxq::gemm;
-  using Cf = PairCfg<FP4>;
-  const int64_t kbytes = Cf::FP4 ? K / 2 : K;
-  const int64_t kb4 = K / 128;
+  using Cf = PairCfg<KIND>;
+  const int64_t kbytes = Cf::FP4 ? g.K / 2 : g.K;
+  const int64_t kb4 = g.K / 128;
   CUtensorMap ma, mb, msa, msb, mc;
-  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, kbytes, M, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+  const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
+  const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
+  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_q, kbytes, arows, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return MXQ_ERR_CUDA;
-  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, kbytes, N, kbytes, BKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_q, kbytes, brows, kbytes, BKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return MXQ_ERR_CUDA;
-  // scales in the tensor-core layout: one 512-byte chunk (128 x 32-bit words) per row
-  if (!encode_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_s, 128, (M / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MXQ_ERR_CUDA;
-  if (!encode_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_s, 128, (N / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MXQ_ERR_CUDA;
-  if (out_fp32) {
-    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M, N * 4, 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+  msa = CUtensorMap{};
+  msb = CUtensorMap{};
+  if (Cf::SCALED) {
+    // scales in the tensor-core layout: one 512-byte chunk (128 x 32-bit words) per row
+    if (!encode_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.a_s, 128, (g.M / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return MXQ_ERR_CUDA;
-  } else {
-    if (!encode_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, N, M, N * 2, 32, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!encode_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.b_s, 128, (g.N / 128) * kb4, 512, 128, Cf::SF_CHUNKS,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return MXQ_ERR_CUDA;
   }
-  Params p{};
-  p.a_s = a_s;
-  p.b_s = b_s;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  p.tiles_m = static_cast<int>(M / 256);
-  p.tiles_n = static_cast<int>(N / 256);
-  p.ntiles = p.tiles_m * p.tiles_n;
-  p.kblocks = static_cast<int>(kbytes / BKB);
-  p.kb4 = static_cast<int>(kb4);
-  p.out_fp32 = out_fp32;
-  p.status = status_ptr();
-  p.a_type = a_type;
-  p.b_type = b_type;
-  p.stall_u = take_test_stall(2) ? 0 : -1;
+  if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
+  Params p = make_params(g, 256, 256, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
   const int grid = 2 * std::min(p.ntiles, pairs);
-  return launch_pdl_cluster(mx_gemm_pair_kernel<FP4>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb,
-                            mc, p);
+  return launch_pdl_cluster(mx_gemm_pair_kernel<KIND>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa,
+                            msb, mc, p);
 }
 
 // The pair kernel for M and N multiples of 256 (when the device can hold it),
 // else the single-CTA kernel.
-template <bool FP4>
-int dispatch(const void* a_q, const uint8_t* a_s, const void* b_q, const uint8_t* b_s, int64_t M, int64_t N,
-             int64_t K, void* c, int out_fp32, uint32_t a_type, uint32_t b_type, cudaStream_t st) {
-  if (M % 256 == 0 && N % 256 == 0) {
-    const int pairs = max_pairs<FP4>(mxq::gemm::mx_gemm_pair_kernel<FP4>, mxq::gemm::PairCfg<FP4>::SMEM);
-    if (pairs > 0) return launch_pair<FP4>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, pairs, st);
+template <int KIND>
+int dispatch(const GemmArgs& g, cudaStream_t st) {
+  if (g.M % 256 == 0 && g.N % 256 == 0) {
+    const int pairs = max_pairs<KIND>(mxq::gemm::mx_gemm_pair_kernel<KIND>, mxq::gemm::PairCfg<KIND>::SMEM);
+    if (pairs > 0) return launch_pair<KIND>(g, pairs, st);
   }
-  return (N % 256 == 0) ? launch<FP4, 256>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, st)
-                        : launch<FP4, 128>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, a_type, b_type, st);
+  return (g.N % 256 == 0) ? launch<KIND, 256>(g, st) : launch<KIND, 128>(g, st);
 }
 
-// Element type code of the block-scaled MMA's instruction descriptor.
-uint32_t mma_type(int fmt) { return fmt == MXQ_E4M3 ? 0u : 1u; }   // E5M2: 1 (mxf8f6f4); E2M1: 1 (mxf4)
+// Element type code of the MMA's instruction descriptor.
+uint32_t mma_type(int fmt) { return fmt == MXQ_E4M3 ? 0u : 1u; }   // E5M2: 1 (mxf8f6f4 / f8f6f4); E2M1: 1 (mxf4)
 
-int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s, int b_fmt,
-                 int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32, void* stream) {
-  if (!a_q || !a_s || !b_q || !b_s || !c) return MXQ_ERR_BAD_ARG;
-  for (int f : {a_fmt, b_fmt})
-    if (f != MXQ_E4M3 && f != MXQ_E5M2 && f != MXQ_E2M1) return MXQ_ERR_BAD_ARG;
+bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E5M2 || f == MXQ_E2M1; }
+
+// Checks shared by the block-scaled entry points; fills g's operand fields.
+int check_mx(GemmArgs& g, const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
+             int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout) {
+  if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_BAD_ARG;
+  if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return MXQ_ERR_BAD_ARG;
   // E2M1 pairs only with E2M1 (kind::mxf4 takes packed FP4 for both operands)
   if ((a_fmt == MXQ_E2M1) != (b_fmt == MXQ_E2M1)) return MXQ_ERR_UNSUPPORTED;
   if (sf_layout != MXQ_SF_MMA) return sf_layout == MXQ_SF_CANONICAL ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
   const bool fp4 = a_fmt == MXQ_E2M1;
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % (fp4 ? 256 : 128)) return MXQ_ERR_BAD_SHAPE;
   if (M > (1ll << 31) - 256 || N > (1ll << 31) - 256 || K > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
-  if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_s) || !aligned16(b_s) || !aligned16(c))
-    return MXQ_ERR_MISALIGNED;
+  if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_s) || !aligned16(b_s)) return MXQ_ERR_MISALIGNED;
+  g = GemmArgs{};
+  g.a_q = a_q;
+  g.a_s = a_s;
+  g.b_q = b_q;
+  g.b_s = b_s;
+  g.batch = 1;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a_type = mma_type(a_fmt);
+  g.b_type = mma_type(b_fmt);
+  return MXQ_OK;
+}
+
+int run_mx(const GemmArgs& g, bool fp4, void* stream) {
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
   auto st = static_cast<cudaStream_t>(stream);
-  return fp4 ? dispatch<true>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, mma_type(a_fmt), mma_type(b_fmt), st)
-             : dispatch<false>(a_q, a_s, b_q, b_s, M, N, K, c, out_fp32, mma_type(a_fmt), mma_type(b_fmt), st);
+  return fp4 ? dispatch<mxq::gemm::KIND_MXF4>(g, st) : dispatch<mxq::gemm::KIND_MXF8>(g, st);
+}
+
+int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s, int b_fmt,
+                 int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32, void* stream) {
+  GemmArgs g;
+  const int rc = check_mx(g, a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout);
+  if (rc != MXQ_OK) return rc;
+  if (!c) return MXQ_ERR_BAD_ARG;
+  if (!aligned16(c)) return MXQ_ERR_MISALIGNED;
+  g.c = c;
+  g.epi = out_fp32 ? mxq::gemm::EPI_FP32 : mxq::gemm::EPI_BF16;
+  return run_mx(g, a_fmt == MXQ_E2M1, stream);
 }
 
 }  // namespace
@@ -848,4 +1056,55 @@ extern "C" int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt, co
                               int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32,
                               void* stream) {
   return gemm_checked(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout, c, out_fp32, stream);
+}
+
+extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
+                               int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, int out_fmt,
+                               int out_scale_mode, int out_sf_layout, uint8_t* c_q, uint8_t* c_s, void* stream) {
+  GemmArgs g;
+  const int rc = check_mx(g, a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout);
+  if (rc != MXQ_OK) return rc;
+  if (!c_q || !c_s) return MXQ_ERR_BAD_ARG;
+  if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2) return out_fmt == MXQ_E2M1 ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
+  if (out_scale_mode != MXQ_SCALE_FLOOR_OCP && out_scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
+  if (out_sf_layout != MXQ_SF_CANONICAL && out_sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
+  if (!aligned16(c_q) || !aligned16(c_s)) return MXQ_ERR_MISALIGNED;
+  g.epi = mxq::gemm::EPI_MX;
+  g.cq = c_q;
+  g.cs = c_s;
+  g.mx_fmt = out_fmt;
+  g.mx_ceil = out_scale_mode == MXQ_SCALE_CEIL;
+  g.mx_sf_mma = out_sf_layout == MXQ_SF_MMA;
+  return run_mx(g, a_fmt == MXQ_E2M1, stream);
+}
+
+extern "C" int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          int a_batched, int b_batched, int fmt, const float* scale, const void* bias, void* c,
+                          void* stream) {
+  if (!a || !b || !scale || !c) return MXQ_ERR_BAD_ARG;
+  if (fmt != MXQ_E4M3 && fmt != MXQ_E5M2) return fmt == MXQ_E2M1 ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
+  if ((a_batched != 0 && a_batched != 1) || (b_batched != 0 && b_batched != 1)) return MXQ_ERR_BAD_ARG;
+  if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 128) return MXQ_ERR_BAD_SHAPE;
+  if (batch * M > (1ll << 31) - 256 || batch * N > (1ll << 31) - 256 || K > (1ll << 31) - 256)
+    return MXQ_ERR_BAD_SHAPE;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (bias && !aligned16(bias)) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  GemmArgs g{};
+  g.a_q = a;
+  g.b_q = b;
+  g.batch = batch;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a_batched = batch > 1 ? a_batched : 0;
+  g.b_batched = batch > 1 ? b_batched : 0;
+  g.a_type = mma_type(fmt);
+  g.b_type = mma_type(fmt);
+  g.epi = mxq::gemm::EPI_BF16;
+  g.c = c;
+  g.alpha = scale;
+  g.bias = bias;
+  return dispatch<mxq::gemm::KIND_F8>(g, static_cast<cudaStream_t>(stream));
 }

@@ -86,30 +86,6 @@ struct QuantParams {
   int stall_tile;     // failure-detection test hook: this tile is never loaded (-1: off)
 };
 
-// destmax = m_d * 2^E_d: exponent and 23-bit mantissa field of the largest
-// finite element (E4M3 1.75*2^8, E5M2 1.75*2^15, E2M1 1.5*2^2).
-template <int FMT> struct FmtInfo;
-template <> struct FmtInfo<MXQ_E4M3> { static constexpr int Ed = 8;  static constexpr uint32_t md = 0x600000u; static constexpr int mbits = 3; static constexpr int emin = -6;  static constexpr float maxv = 448.f; };
-template <> struct FmtInfo<MXQ_E5M2> { static constexpr int Ed = 15; static constexpr uint32_t md = 0x600000u; static constexpr int mbits = 2; static constexpr int emin = -14; static constexpr float maxv = 57344.f; };
-template <> struct FmtInfo<MXQ_E2M1> { static constexpr int Ed = 2;  static constexpr uint32_t md = 0x400000u; static constexpr int mbits = 1; static constexpr int emin = 0;   static constexpr float maxv = 6.f; };
-
-// Shared exponent e from the block amax given as float32 bits (>= 0, finite;
-// bf16 values are exact float32): floor rule e = E(amax) - E(destmax); ceil
-// rule adds 1 when amax's mantissa field exceeds destmax's.  A zero or
-// subnormal amax has E <= -127, so with E(destmax) >= 2 the clamp to
-// [-127, 127] gives -127 -- the amax == 0 rule -- without special cases.
-template <int FMT>
-__device__ __forceinline__ int scale_exp(uint32_t ab, int ceil_mode) {
-  int e = static_cast<int>(ab >> 23) - 127 - FmtInfo<FMT>::Ed;
-  if (ceil_mode && (ab & 0x7FFFFFu) > FmtInfo<FMT>::md) e += 1;
-  return max(-127, min(127, e));
-}
-
-// 2^-e as float32 (e in [-127, 125] here, so the result is a normal number).
-__device__ __forceinline__ float exp2_neg(int e) {
-  return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-}
-
 // Stochastic rounding of y (float32, exact) to the element grid with the
 // 32-bit draw r: magnitude y' = min(|y|, max) between grid neighbours
 // lo <= y' < lo + sp rounds up iff r < floor((y' - lo) / sp * 2^32).  All

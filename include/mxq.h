@@ -181,6 +181,43 @@ int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt,
                    int64_t M, int64_t N, int64_t K, int sf_layout, void* c,
                    int out_fp32, void* stream);
 
+/* ---- block-scaled GEMM with an MX output (FAF article: producers emit the
+ * format and scale layout their consumer reads, with no bf16 round trip) -----
+ * Same product as mxq_gemm_mixed.  Instead of C, writes
+ *   c_q [M][N] codes of out_fmt (MXQ_E4M3 | MXQ_E5M2), and
+ *   c_s the UE8M0 scales of the 1x32 blocks along each row of C:
+ *       canonical [M][N/32], or MXQ_SF_MMA (the layout mxq_gemm reads for
+ *       an A operand).
+ * The block scale (out_scale_mode MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL) and
+ * the RNE-saturating element rounding follow mxq_quantize, applied to the
+ * float32 accumulator.  A block holding NaN/Inf gets scale 0xFF and zero
+ * codes.  c_q and c_s 16-byte aligned.  E2M1 output: MXQ_ERR_UNSUPPORTED. */
+int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt,
+                    const void* b_q, const uint8_t* b_s, int b_fmt,
+                    int64_t M, int64_t N, int64_t K, int sf_layout,
+                    int out_fmt, int out_scale_mode, int out_sf_layout,
+                    uint8_t* c_q, uint8_t* c_s, void* stream);
+
+/* ---- per-tensor FP8 GEMM (AstrAI fp8.py, mm_fp8: "a @ b * scale (+ bias)",
+ * scale the combined dequantization scale, bias added in the fp32 epilogue,
+ * bf16 result) -------------------------------------------------------------------
+ * c[i][m][n] = bf16_RNE( RN32( RN32(acc * scale) + bias[n] ) ), acc the
+ * float32 tensor-core sum over k of dec(a[i][m][k]) * dec(b[i][n][k]).
+ * a        FP8 codes, [batch][M][K] when a_batched, else [M][K] shared by
+ *          every batch entry (K-contiguous rows).
+ * b        FP8 codes, [batch][N][K] when b_batched, else [N][K] (the
+ *          transposed view of a [K][N] operand: K-contiguous rows).
+ * fmt      MXQ_E4M3 | MXQ_E5M2 for both operands.
+ * scale    device float (4-byte aligned), read by the kernel.
+ * bias     NULL or device bf16 [N], 16-byte aligned.
+ * c        bf16 [batch][M][N], 16-byte aligned.
+ * batch >= 1; M, N, K multiples of 128.  Operands with M- or N-contiguous
+ * rows are not taken (the per-tensor quantizer's transposed output gives the
+ * K-contiguous copy). */
+int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M,
+               int64_t N, int64_t K, int a_batched, int b_batched, int fmt,
+               const float* scale, const void* bias, void* c, void* stream);
+
 /* ---- scale layout conversion ([FAF]) -----------------------------------------
  * Canonical scales s [rows][kb] -> MMA layout (rows % 128 == 0,
  * kb % 4 == 0).  out holds rows*kb bytes; must not overlap s. */

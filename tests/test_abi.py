@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed", "mxq_sf_to_mma",
+    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed",
+              "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
               "mxq_last_device_status", "mxq_strerror", "mxq_version"):
         assert n in names
 
@@ -91,6 +92,22 @@ def test_argument_checks_need_no_gpu(so):
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 5, 128, 128, 256, 1, FAKE, 0, None) == -1   # unknown format
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 100, 128, 256, 1, FAKE, 0, None) == -2
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 128, 128, 256, 0, FAKE, 0, None) == -4   # canonical scales
+
+    mo = so.mxq_gemm_mx_out
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 2, 0, 0, FAKE, FAKE, None) == -4   # E2M1 output
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 2, 0, FAKE, FAKE, None) == -1   # scale mode
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 2, FAKE, FAKE, None) == -1   # scale layout
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, FAKE, None, None) == -1   # no scales
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, ODD, FAKE, None) == -3
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 100, 128, 1, 0, 0, 0, FAKE, FAKE, None) == -2
+
+    mm = so.mxq_mm_fp8
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 2, FAKE, None, FAKE, None) == -4   # E2M1
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, None, None, FAKE, None) == -1   # no scale
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 2, 0, 0, FAKE, None, FAKE, None) == -1   # batched flag
+    assert mm(FAKE, FAKE, 0, 128, 128, 128, 0, 0, 0, FAKE, None, FAKE, None) == -2   # batch 0
+    assert mm(FAKE, FAKE, 1, 100, 128, 128, 0, 0, 0, FAKE, None, FAKE, None) == -2
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, FAKE, ODD, FAKE, None) == -3   # bias alignment
 
     assert so.mxq_dequantize(FAKE, FAKE, 64, 48, 0, 1, FAKE, None) == -2
     assert so.mxq_sf_to_mma(FAKE, 100, 4, FAKE, None) == -2

@@ -1,0 +1,184 @@
+"""GPU parity of the GEMM's other outputs: the MX-quantized output (codes and
+UE8M0 scales of 1x32 row blocks written from the accumulator) and the
+per-tensor FP8 product with scale and bias (mm_fp8).
+
+Operands come from the CPU oracle.  Where the float32 accumulation is exact
+(small-integer sums), the MX output must equal the oracle's MX quantization
+of the float64 product bit for bit; elsewhere the decisions are taken on the
+kernel's float32 accumulator, which the oracle cannot reproduce, so the
+check is a property that holds at any size: the dequantized output sits
+within one element step of the float64 product and nearly every code
+agrees.  The per-tensor product passes the 2e-3 gate (oracle.gemm).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_02_gb300 import inputs
+from oracle import formats as F
+from oracle import gemm as og
+from oracle import mx as omx
+from tests.helpers import assert_bytes_equal, f64
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2}
+MODES = {"floor": omx.FLOOR, "ceil": omx.CEIL}
+dev = torch.device("cuda")
+
+
+def t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def mx_operand(x, fmt):
+    r = omx.quantize(x, FMTS[fmt], omx.ROW, omx.FLOOR)
+    return r["q_row"], r["s_row"]
+
+
+def run_mx_out(lib, aq, as_, bq, bs, fmt, out_fmt, mode, layout):
+    cq, cs = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt,
+                                out_fmt=out_fmt, out_scale_mode=mode, out_sf_layout=layout)
+    cq = cq.cpu().numpy()
+    cs = cs.cpu().numpy()
+    if layout == "mma":
+        cs = omx.sf_from_mma(cs.reshape(-1), cq.shape[0], cq.shape[1] // 32)
+    return cq, cs
+
+
+@pytest.mark.parametrize("out_fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("mode", ["floor", "ceil"])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+@pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 1024), (128, 384, 256)])
+def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk):
+    """A = +-2^j per row (exact in E4M3 with the row scale), B = small
+    integers: every product and partial sum is exact in float32, so the
+    accumulator equals the float64 product and the MX output must equal the
+    oracle's quantization of it, codes and scales."""
+    M, N, K = mnk
+    rng = np.random.default_rng(21)
+    a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
+    b = rng.integers(-4, 5, (N, K)).astype(np.float64)
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    ref = og.reference(aq, as_, bq, bs, F.E4M3)
+    assert np.array_equal(ref, a @ b.T)                          # the operands quantize exactly
+    want = omx.quantize(ref, FMTS[out_fmt], omx.ROW, MODES[mode])
+    cq, cs = run_mx_out(lib, aq, as_, bq, bs, "e4m3", out_fmt, mode, layout)
+    assert_bytes_equal(cq, want["q_row"], "codes")
+    assert_bytes_equal(cs, want["s_row"], "scales")
+
+
+def e4m3_spacing(y):
+    """Grid spacing of E4M3 at magnitude y (3 mantissa bits; subnormal step 2^-9)."""
+    a = np.abs(y)
+    safe = np.where(a >= 2.0 ** -6, a, 1.0)
+    return np.where(a >= 2.0 ** -6, np.exp2(np.floor(np.log2(safe)) - 3), 2.0 ** -9)
+
+
+@pytest.mark.parametrize("mnk", [(256, 512, 1024), (384, 256, 2048)])
+def test_mx_output_random_within_one_step(lib, mnk):
+    """Random activations x weights: the kernel quantizes its float32
+    accumulator, the oracle the float64 product, so decisions may differ
+    where a value sits on a rounding or binade boundary.  Scales differ by
+    at most one binade; where they agree the element codes differ by at most
+    one grid step; elsewhere the dequantized values differ by at most one
+    top-binade step; and at least 99 % of the codes are equal."""
+    M, N, K = mnk
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    ref = og.reference(aq, as_, bq, bs, F.E4M3)
+    want = omx.quantize(ref, F.E4M3, omx.ROW, omx.FLOOR)
+    cq, cs = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e4m3", "floor", "canonical")
+    ek = cs.astype(int) - 127
+    eo = want["s_row"].astype(int) - 127
+    assert np.max(np.abs(ek - eo)) <= 1
+    same = np.repeat(ek == eo, 32, axis=1)
+    yk = F.decode(F.E4M3, cq)
+    yo = F.decode(F.E4M3, want["q_row"])
+    tol = e4m3_spacing(np.maximum(np.abs(yk), np.abs(yo)))
+    assert np.all(np.abs(yk - yo)[same] <= tol[same])
+    dk = omx.dequantize(cq, cs, F.E4M3)
+    do = omx.dequantize(want["q_row"], want["s_row"], F.E4M3)
+    top = np.repeat(np.exp2(np.maximum(ek, eo) + 5.0), 32, axis=1)
+    assert np.all(np.abs(dk - do)[~same] <= top[~same])
+    assert np.mean(cq == want["q_row"]) >= 0.99
+
+
+def test_mx_output_feeds_the_next_gemm(lib):
+    """Producer writes its consumer's layout: the MMA-layout output of one
+    GEMM is the A operand of the next, with no conversion in between."""
+    M, N, K, N2 = 256, 512, 512, 256
+    rng = np.random.default_rng(22)
+    a = rng.choice([-1.0, 1.0], (M, K))
+    b = rng.integers(-2, 3, (N, K)).astype(np.float64)
+    w = rng.choice([-1.0, 1.0], (N2, N))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    wq, ws = mx_operand(w, "e4m3")
+    cq, cs = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), "e4m3",
+                                out_sf_layout="mma")
+    d = lib.mx_gemm(cq, cs, t(wq), t(omx.sf_to_mma(ws)), "e4m3", torch.float32)
+    c_ref = omx.quantize(a @ b.T, F.E4M3, omx.ROW, omx.FLOOR)
+    d_ref = og.reference(c_ref["q_row"], c_ref["s_row"], wq, ws, F.E4M3)
+    assert og.gate_error(d.cpu().numpy().astype(np.float64), d_ref, out_is_bf16=False) <= 1e-5
+
+
+# ---------------------------------------------------------------- mm_fp8
+def fp8_codes(x, fmt):
+    return F.encode_rne_sat(FMTS[fmt], x)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 512)])
+def test_mm_fp8_one_hot_rows_exact(lib, fmt, mnk):
+    """One-hot A rows pick B's columns; with scale 0.5 and no bias every
+    output is an FP8 value times 0.5, exact in bf16."""
+    M, N, K = mnk
+    rng = np.random.default_rng(23)
+    a8 = np.zeros((M, K), dtype=np.uint8)
+    a8[np.arange(M), rng.integers(0, K, M)] = fp8_codes(np.array([1.0]), fmt)[0]
+    b8 = fp8_codes(rng.standard_normal((N, K)) * 8, fmt)
+    scale = torch.tensor([0.5], dtype=torch.float32, device=dev)
+    c = lib.mm_fp8(t(a8), t(b8), scale, trans_b=True, fmt=fmt)
+    ref = og.mm_fp8_reference(a8, b8, FMTS[fmt], 0.5)
+    assert np.array_equal(c.float().cpu().numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("shape", [(1, 256, 512, 1024), (3, 256, 256, 512), (2, 128, 384, 256)])
+@pytest.mark.parametrize("b_batched", [False, True])
+def test_mm_fp8_gate_with_bias_and_batches(lib, fmt, shape, b_batched):
+    batch, M, N, K = shape
+    rng = np.random.default_rng(24)
+    a8 = fp8_codes(rng.standard_normal((batch, M, K)), fmt)
+    b8 = fp8_codes(rng.standard_normal((batch, N, K) if b_batched else (N, K)) * 2, fmt)
+    bias = inputs.to_bf16(rng.standard_normal(N).astype(np.float32))
+    sc = np.float32(0.0123)
+    scale = torch.tensor([sc], dtype=torch.float32, device=dev)
+    c = lib.mm_fp8(t(a8), t(b8).transpose(-1, -2), scale, bias=bias.to(dev), fmt=fmt)
+    ref = og.mm_fp8_reference(a8, b8, FMTS[fmt], float(sc), f64(bias))
+    got = c.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape
+    assert og.gate_error(got, ref) <= 2e-3
+
+
+def test_mm_fp8_views_fold_and_bad_layouts_raise(lib):
+    rng = np.random.default_rng(25)
+    a8 = t(fp8_codes(rng.standard_normal((256, 256)), "e4m3"))
+    w8 = t(fp8_codes(rng.standard_normal((256, 256)), "e4m3"))
+    scale = torch.tensor([1.0], dtype=torch.float32, device=dev)
+    c1 = lib.mm_fp8(a8, w8, scale, trans_b=True)
+    c2 = lib.mm_fp8(a8, w8.t(), scale)
+    assert torch.equal(c1, c2)
+    with pytest.raises(ValueError):
+        lib.mm_fp8(a8, w8, scale)                                # row-major [K][N] b: N-contiguous
+    with pytest.raises(ValueError):
+        lib.mm_fp8(a8, w8, scale, trans_a=True, trans_b=True)   # op(a) M-contiguous
+
+
+def test_device_status_clean_after_epilogues(lib):
+    assert lib.last_device_status() == 0
