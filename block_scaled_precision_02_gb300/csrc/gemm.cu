@@ -613,7 +613,10 @@ struct PairCfg {
   static constexpr int SFB_COLS = 8 * SF_CHUNKS;
   static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_COLS = 512;
-  static_assert(BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
+  // without block scales two accumulators fit: the epilogue drains one
+  // while the MMAs fill the other
+  static constexpr int NACC = SCALED ? 1 : 2;
+  static_assert(NACC * BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
   static constexpr int SMEM = STAGES * TX_CTA + 2 * STG_BYTES + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -643,6 +646,11 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   volatile int* epi_fail = reinterpret_cast<volatile int*>(acc_full + 3) + 2;
   uint64_t* sf_full = acc_full + 5;                            // rank 0: a slot's scales are in tensor memory
   uint64_t* sf_drain = sf_full + STAGES_P;                     // rank 0
+  // accumulator buffer b: full / empty barriers (the second pair exists when NACC == 2)
+  uint64_t* const acc_full1 = sf_drain + 1;
+  uint64_t* const acc_empty1 = sf_drain + 2;                   // used in rank 0
+  auto accf = [&](int b) { return b ? acc_full1 : acc_full; };
+  auto acce = [&](int b) { return b ? acc_empty1 : acc_empty; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -658,6 +666,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < STAGES_P; ++s) mbar_init(smem_u32(&sf_full[s]), 1);
     mbar_init(smem_u32(sf_drain), 1);
+    mbar_init(smem_u32(acc_full1), 1);
+    mbar_init(smem_u32(acc_empty1), 8);
     *abort_flag = 0;
     *epi_fail = 0;
     fence_mbar_init();
@@ -731,7 +741,10 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       bool ok = true;
       int s = 0, ph = 0;
       for (int t = 0; t < my_tiles && ok && !*abort_flag; ++t) {
-        if (!mbar_wait_suspend(smem_u32(acc_empty), (t & 1) ^ 1, p.status)) { ok = false; break; }
+        const int ab = C::NACC == 2 ? (t & 1) : 0;            // accumulator buffer and its use parity
+        const uint32_t aph = C::NACC == 2 ? ((t >> 1) & 1) : (t & 1);
+        const uint32_t dacc = tmem + ab * C::BN;
+        if (!mbar_wait_suspend(smem_u32(acce(ab)), aph ^ 1, p.status)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < p.kblocks; ++kb) {
           if (!mbar_wait_suspend(smem_u32(&ready[s]), ph, p.status)) { ok = false; break; }
@@ -744,13 +757,13 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 8 * (kk >> 1) : sfb_t;
-            tc_mma_pair<KIND>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma_pair<KIND>(dacc, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit_pair_both(smem_u32(&empty[s]));            // stage free in both CTAs
           if (++s == STAGES_P) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        tc_commit_pair_both(smem_u32(acc_full));                // both halves of the accumulator ready
+        tc_commit_pair_both(smem_u32(accf(ab)));                // both halves of the accumulator ready
       }
       if (!ok) *abort_flag = 1;
       tc_commit_pair_self(smem_u32(drain));
@@ -793,19 +806,23 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const int q = warp & 3;
     const bool leader = (warp == EPI_WARP0 && lane == 0);
     const uint32_t acc_empty_r0 = cluster_map(smem_u32(acc_empty), 0);
+    const uint32_t acc_empty1_r0 = cluster_map(smem_u32(acc_empty1), 0);
     const float alpha = (C::KIND == KIND_F8 && p.alpha) ? *p.alpha : 1.0f;
     int t = 0, buf = 0;
     for (int tile = pair; tile < p.ntiles; tile += npairs, ++t) {
       const TilePos tp = tile_pos(p, tile, 256, 256);
       const int m0 = tp.b * p.M + tp.m0 + static_cast<int>(rank) * BM;   // rows of the batched output
-      if (!mbar_wait_suspend(smem_u32(acc_full), t & 1, p.status)) *epi_fail = 1;
+      const int ab = C::NACC == 2 ? (t & 1) : 0;
+      const uint32_t aph = C::NACC == 2 ? ((t >> 1) & 1) : (t & 1);
+      if (!mbar_wait_suspend(smem_u32(accf(ab)), aph, p.status)) *epi_fail = 1;
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<C::BN, C::KIND == KIND_F8>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, m0, tp.n0, [&] {
+      store_tile<C::BN, C::KIND == KIND_F8>(p, alpha, tmem + ab * C::BN, q, lane, leader, buf, sOut, &map_c, m0,
+                                            tp.n0, [&] {
         if (lane == 0) {
-          if (rank == 0) mbar_arrive(smem_u32(acc_empty));
-          else mbar_arrive_remote(acc_empty_r0);
+          if (rank == 0) mbar_arrive(smem_u32(acce(ab)));
+          else mbar_arrive_remote(ab ? acc_empty1_r0 : acc_empty_r0);
         }
       });
     }

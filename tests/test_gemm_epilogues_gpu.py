@@ -166,6 +166,20 @@ def test_mm_fp8_gate_with_bias_and_batches(lib, fmt, shape, b_batched):
     assert og.gate_error(got, ref) <= 2e-3
 
 
+def test_mm_fp8_more_tiles_than_pairs(lib):
+    """4 x 2048 x 2048 outputs are 256 tiles of 256 x 256, more than the CTA
+    pairs, so each pair alternates between its two accumulators."""
+    rng = np.random.default_rng(26)
+    batch, M, N, K = 4, 2048, 2048, 256
+    a8 = fp8_codes(rng.standard_normal((batch, M, K)), "e4m3")
+    b8 = fp8_codes(rng.standard_normal((N, K)), "e4m3")
+    bias = inputs.to_bf16(rng.standard_normal(N).astype(np.float32))
+    scale = torch.tensor([0.5], dtype=torch.float32, device=dev)
+    c = lib.mm_fp8(t(a8), t(b8), scale, trans_b=True, bias=bias.to(dev), fmt="e4m3")
+    ref = og.mm_fp8_reference(a8, b8, F.E4M3, 0.5, f64(bias))
+    assert og.gate_error(c.float().cpu().numpy().astype(np.float64), ref) <= 2e-3
+
+
 def test_mm_fp8_views_fold_and_bad_layouts_raise(lib):
     rng = np.random.default_rng(25)
     a8 = t(fp8_codes(rng.standard_normal((256, 256)), "e4m3"))
