@@ -356,6 +356,29 @@ def small_part(args, mxq, X, timed):
     return ms1q, ms1d, 2 * args.steps
 
 
+def alu_roofline(key: str, elems: int, ms: float, sm_mhz: float):
+    """Integer-issue roofline of an ALU-bound quantizer path: the thread
+    instructions it executes per element (profiles/alu.json, from one ncu
+    capture of the same kernel source) times the elements per second, against
+    the issue peak of the SMs (4 schedulers x 32 lanes, one instruction per
+    clock each, at the maximum SM clock).  None once the kernel source
+    differs from the captured one."""
+    p = os.path.join(ROOT, "profiles", "alu.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        e = json.load(fh).get(f"quant_tiles_kernel {key}")
+    if not e or e.get("source_sha") != source_sha("quantize.cu"):
+        return None
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    achieved = e["inst_per_element"] * elems / (ms * 1e-3)
+    peak = sms * 128 * sm_mhz * 1e6
+    return {"bound": "alu", "achieved": round(achieved / 1e12, 2), "peak": round(peak / 1e12, 2),
+            "unit": "T thread-instructions/s", "frac": round(achieved / peak, 4),
+            "inst_per_element": e["inst_per_element"], "peak_source": f"{sms} SMs x 128 lanes x {sm_mhz:.0f} MHz"}
+
+
 def hbm_row(nbytes, ms, hbm, note=None):
     gbs = nbytes / (ms * 1e-3) / 1e9
     r = {"ms": round(ms, 4), "gbs": round(gbs, 1),
@@ -410,6 +433,7 @@ def run_ours(args, rank, world):
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     bf16 = float(peaks["bf16_tflops"])
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
 
     # L2 flush: write a 256 MiB buffer (twice the 129 MB L2), then read it
     # back so the dirty lines are written out here, outside the timed pair,
@@ -577,10 +601,12 @@ def run_ours(args, rank, world):
         "gemm": {"metric": "MX GEMM TFLOP/s", "rows": gemm_rows, "cpu_baseline": gcpu},
         "rows": {
             "pertensor_fp8_ring_4096x14336_dual": hbm_row(b3, ms3, hbm),
-            "mxfp4_hadamard_sr_quantize_4096x14336": hbm_row(
+            "mxfp4_hadamard_sr_quantize_4096x14336": dict(hbm_row(
                 b_q5, ms_q5[0], hbm, "one Philox-4x32-10 draw per element: integer-ALU bound"),
-            "mxfp4_hadamard_sr4_quantize_4096x14336": hbm_row(
+                alu_roofline=alu_roofline("sr_hadamard_e2m1_4096x14336", 4096 * 14336, ms_q5[0], sm_max)),
+            "mxfp4_hadamard_sr4_quantize_4096x14336": dict(hbm_row(
                 b_q5, ms_q5[1], hbm, "option SR4: four draws per Philox-4x32-10 call"),
+                alu_roofline=alu_roofline("sr4_hadamard_e2m1_4096x14336", 4096 * 14336, ms_q5[1], sm_max)),
             "small_rowwise_256x512": {"quantize_us": round(ms1q * 1e3, 2), "dequantize_us": round(ms1d * 1e3, 2)},
         },
         "cpu_baseline": cpu,
