@@ -100,7 +100,8 @@ extern "C" {
 /* ---- MX quantize ([MX] sections 1 and 4, gap sections 1-2; [FAF]) ----------
  * x        bf16 [rows][ld] (only the first cols of each row are read),
  *          16-byte aligned, ld % 8 == 0, ld >= cols.
- * rows, cols  multiples of 32 (rows % 128 and cols % 128 for SF_MMA;
+ * rows, cols  positive multiples of 32 (an empty tensor is MXQ_ERR_BAD_SHAPE;
+ *          rows % 128 and cols % 128 for SF_MMA;
  *          cols % 2... E2M1 needs even counts along the packed axis, given).
  * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1.
  * orient   MXQ_ROW | MXQ_COL | MXQ_DUAL.
@@ -164,7 +165,8 @@ int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
  * a_q [M][K] codes, b_q [N][K] codes (both K-contiguous; E2M1 packed
  *          [M][K/2], [N][K/2]); a_s, b_s scales in MXQ_SF_MMA layout.
  * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1 (same for both operands).
- * M % 128 == 0, N % 128 == 0, K % 128 == 0 (E2M1: K % 256 == 0).
+ * M, N, K positive; M % 128 == 0, N % 128 == 0, K % 128 == 0 (E2M1:
+ * K % 256 == 0).  Zero sizes are MXQ_ERR_BAD_SHAPE.
  * c [M][N], 16-byte aligned. */
 int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q,
              const uint8_t* b_s, int64_t M, int64_t N, int64_t K, int fmt,

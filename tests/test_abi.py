@@ -68,6 +68,12 @@ def test_argument_checks_need_no_gpu(so):
     assert q(FAKE, 48, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
     assert q(FAKE, 64, 64, 32, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
     assert q(FAKE, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 1, FAKE, FAKE, None, None, None) == -2
+    # empty tensors are a shape error, checked before any launch
+    assert q(FAKE, 0, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
+    assert q(FAKE, 64, 0, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -2
+    assert so.mxq_gemm(FAKE, FAKE, FAKE, FAKE, 0, 128, 128, 0, 1, FAKE, 0, None) == -2
+    assert so.mxq_gemm(FAKE, FAKE, FAKE, FAKE, 128, 128, 0, 0, 1, FAKE, 0, None) == -2
+    assert so.fp8_quantize_pertensor(FAKE, 0, 64, FAKE, 0, 1, None, 0, 0, 448.0, 1.0, FAKE, None, FAKE, None) == -2
     # misaligned input or leading dimension
     assert q(ODD, 64, 64, 64, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -3
     assert q(FAKE, 64, 64, 68, 0, 1, 0, 0, 0, 0, 7, 0, FAKE, FAKE, None, None, None) == -3

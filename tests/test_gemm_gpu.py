@@ -59,7 +59,7 @@ def test_unit_rows_select_columns_exactly(lib, fmt, mn):
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
 @pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 1024), (384, 384, 512), (128, 128, 2048),
-                                 (768, 512, 768), (256, 256, 4096)])
+                                 (768, 512, 768), (256, 256, 4096), (128, 128, 256), (256, 256, 256)])
 def test_random_gemm_gate(lib, fmt, mnk):
     M, N, K = mnk
     a = f64(inputs.activations(M, K, seed=0))
