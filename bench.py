@@ -275,6 +275,11 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     fn = lambda: mxq.mx_gemm_mx_out(aq, as_, wq, ws, "e4m3", out_fmt="e4m3", out_sf_layout="mma")
     n += extra_gemm_row(args, fn, timed, "mxfp8_gemm_mx_e4m3_out_8192x4096x4096", M, 4096, K, bf16, peak_src,
                         gemm_rows)
+    # row and transposed column blocks together (the copies a backward pass reads)
+    fn = lambda: mxq.mx_gemm_mx_out(aq, as_, wq, ws, "e4m3", out_fmt="e4m3", out_sf_layout="mma",
+                                    orientation="dual")
+    n += extra_gemm_row(args, fn, timed, "mxfp8_gemm_mx_e4m3_dual_out_8192x4096x4096", M, 4096, K, bf16, peak_src,
+                        gemm_rows)
     # per-tensor FP8 product with scale and bias (mm_fp8): the per-tensor
     # quantizer's E4M3 activations times E4M3 weights
     x8 = mxq.fp8_quantize_pertensor(X["A"], X["one"], "e4m3", "row")[0]

@@ -59,7 +59,7 @@ def load() -> ctypes.CDLL:
     L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
     L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
     L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
-    L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp]
+    L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
     L.mxq_last_device_status.argtypes = [vp]
@@ -218,24 +218,33 @@ def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.
 
 def mx_gemm_mx_out(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.Tensor, fmt="e4m3",
                    b_fmt=None, out_fmt="e4m3", out_scale_mode="floor", out_sf_layout="canonical",
-                   K: Optional[int] = None):
-    """A * B^T as mx_gemm, written as MX codes and scales of 1x32 row blocks
-    (out_fmt, out_scale_mode, out_sf_layout) straight from the accumulator.
-    Returns (codes uint8 [M][N], scales uint8 [M][N/32] or the MMA-layout
-    bytes)."""
+                   orientation="row", K: Optional[int] = None):
+    """A * B^T as mx_gemm, written as MX codes and scales straight from the
+    accumulator: row blocks (1x32 along N) and/or column blocks (32x1 along
+    M, stored transposed), per ``orientation`` ("row", "col", "dual").
+    Returns (codes [M][N], scales [M][N/32], codesT [N][M], scalesT [N][M/32])
+    with None for an orientation not requested; MMA-layout scales hold the
+    same number of bytes."""
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
+    o = _ORIENT[orientation]
     M = a_q.shape[0]
     N = b_q.shape[0]
     if K is None:
         K = a_q.shape[1] * (2 if f == E2M1 else 1)
     dev = a_q.device
-    cq = torch.empty(M, N, dtype=torch.uint8, device=dev)
-    cs = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
+    cq = cs = cqT = csT = None
+    if o & ROW:
+        cq = torch.empty(M, N, dtype=torch.uint8, device=dev)
+        cs = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
+    if o & COL:
+        cqT = torch.empty(N, M, dtype=torch.uint8, device=dev)
+        csT = torch.empty(N, M // 32, dtype=torch.uint8, device=dev)
     rc = load().mxq_gemm_mx_out(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, SF_MMA, _FMT[out_fmt],
-                                _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _stream(dev))
+                                _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _ptr(cqT),
+                                _ptr(csT), _stream(dev))
     _check(rc, "mxq_gemm_mx_out")
-    return cq, cs
+    return cq, cs, cqT, csT
 
 
 def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool = False, trans_b: bool = False,

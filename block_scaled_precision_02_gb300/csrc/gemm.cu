@@ -54,6 +54,10 @@ constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int PAIR_THREADS = 224;     // pair kernel: the roles above plus warp 6 (scale copies)
 constexpr int STG_BYTES = BM * 64;       // one staging buffer: 128 rows x 64 B
+// the staging area: two buffers, also the 4 warps' 32 x 33-word transpose
+// scratch of the MX column-block output
+constexpr int OUT_BYTES = 2 * STG_BYTES + 512;
+static_assert(4 * 32 * 33 * 4 <= OUT_BYTES, "transpose scratch");
 
 // Operand kinds (a template parameter of both kernels).
 constexpr int KIND_MXF8 = 0;   // block-scaled E4M3 / E5M2: kind::mxf8f6f4, scale_vec::1X
@@ -78,6 +82,8 @@ struct Params {
   const __nv_bfloat16* bias;      // per-tensor kind: bias[N] or nullptr
   uint8_t* cq;                    // EPI_MX: codes [M][N]
   uint8_t* cs;                    // EPI_MX: scales, canonical [M][N/32] or the MMA layout
+  uint8_t* cqT;                   // EPI_MX column blocks: codes of C^T [N][M] (or nullptr)
+  uint8_t* csT;                   // EPI_MX column blocks: scales, canonical [N][M/32] or the MMA layout
   int mx_fmt, mx_ceil, mx_sf_mma;
   int* status;
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
@@ -265,6 +271,45 @@ __device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt,
   return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
 }
 
+// The same for column `lane` of a warp's 32 x 32 chunk held in shared memory
+// (word k * 33 + j holds row k, column j; the padding keeps both the row
+// writes and the column reads free of bank conflicts): the block's 32 values
+// are read twice (amax, then codes) so that few registers are live.
+__device__ __forceinline__ uint32_t mx_block32_col(const uint32_t* xs, int lane, int fmt, int ceil_mode,
+                                                   uint32_t* codes /* 8 words */) {
+  uint32_t ab = 0;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) ab = max(ab, xs[k * 33 + lane] & 0x7FFFFFFFu);
+  const bool bad = ab >= 0x7F800000u;
+  const int e = bad ? 0 : (fmt == MXQ_E4M3 ? scale_exp<MXQ_E4M3>(ab, ceil_mode) : scale_exp<MXQ_E5M2>(ab, ceil_mode));
+  const float m = exp2_neg(e);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    float f[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __fmul_rn(__uint_as_float(xs[(4 * w + i) * 33 + lane]), m);
+    codes[w] = bad ? 0u : fp8x4_rt(fmt, f[0], f[1], f[2], f[3]);
+  }
+  return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+}
+
+// Row-block scale words of one output row (BN / 32 scale bytes, four per
+// word, scale columns n0 / 32 ..) in the canonical or the MMA layout.
+template <int BN>
+__device__ __forceinline__ void store_row_scales(const Params& p, size_t rg, int n0, const uint32_t (&sc)[BN / 128]) {
+  const int kb = p.N / 32;                                       // scale columns
+#pragma unroll
+  for (int g = 0; g < BN / 128; ++g) {
+    const int j0 = n0 / 32 + 4 * g;                              // first scale column of this word
+    size_t off;
+    if (p.mx_sf_mma)                                             // chunk (rg/128, j0/4), row rg%32, word (rg/32)%4
+      off = ((rg / 128) * static_cast<size_t>(kb / 4) + j0 / 4) * 512 + (rg % 32) * 16 + ((rg / 32) % 4) * 4;
+    else
+      off = rg * static_cast<size_t>(kb) + j0;
+    *reinterpret_cast<uint32_t*>(p.cs + off) = sc[g];
+  }
+}
+
 // Epilogue of one output tile: drain this CTA's 128 x BN float32
 // accumulator (tensor-memory lanes 0..127, columns 0..BN-1; the thread of
 // lane quarter q and lane `lane` owns row 32 q + lane), call release() once
@@ -272,13 +317,13 @@ __device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt,
 // whole batched output) in the mode p.epi.  bf16 / float32 go through two
 // 64-byte-swizzled staging buffers and TMA stores issued by `leader`; all
 // 128 epilogue threads take part (named barrier 1).
-template <int BN, bool PER_TENSOR, typename Release>
+template <int BN, bool PER_TENSOR, int MXOUT, typename Release>
 __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_t tmem, int q, int lane, bool leader,
                                            int& buf, uint8_t* sOut, const CUtensorMap* map_c, int m0, int n0,
                                            Release release) {
   const int row = q * 32 + lane;
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-  if (p.epi == EPI_BF16) {
+  if (MXOUT == 0 && p.epi == EPI_BF16) {
     // drain the whole accumulator row into registers first, so the MMA warp
     // can start the next tile while this one is written out (two 32-column
     // loads in flight per wait)
@@ -332,9 +377,10 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     }
     return;
   }
-  if (p.epi == EPI_MX) {
-    // each 32-column chunk of a row is one MX block: codes and the scale
-    // byte are formed from the registers, then stored straight to memory
+  if constexpr (MXOUT == 1) {
+    // row blocks only: each 32-column chunk of a row is one MX block; codes
+    // and scale bytes are formed in registers, the accumulator is released,
+    // and then they are stored
     uint32_t codes[BN / 4];
     uint32_t sc[BN / 128];
 #pragma unroll
@@ -358,17 +404,61 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     uint4* dst = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0);
 #pragma unroll
     for (int i = 0; i < BN / 16; ++i) dst[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
-    const int kb = p.N / 32;                                     // scale columns
+    store_row_scales<BN>(p, rg, n0, sc);
+    return;
+  }
+  if constexpr (MXOUT == 2) {
+    // row blocks: each 32-column chunk of a row is one MX block, formed
+    // from the registers and stored at once (only the scale words are kept
+    // to the end).  Column blocks: a warp's 32 rows of a chunk are 32 blocks
+    // of 32 x 1; the warp transposes the chunk through its part of the (here
+    // unused) staging area, rows padded to 33 words so that neither the row
+    // writes nor the column reads conflict, and lane j quantizes column j.
+    uint32_t sc[BN / 128];
+    uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * (32 * 33);   // this warp's 32 x 33 words
+    const size_t rg = static_cast<size_t>(m0 + row);
+    const size_t rT = static_cast<size_t>(m0 + q * 32);          // first row of the warp's column blocks
 #pragma unroll
-    for (int g = 0; g < BN / 128; ++g) {
-      const int j0 = n0 / 32 + 4 * g;                            // first scale column of this word
-      size_t off;
-      if (p.mx_sf_mma)                                           // chunk (rg/128, j0/4), row rg%32, word (rg/32)%4
-        off = ((rg / 128) * static_cast<size_t>(kb / 4) + j0 / 4) * 512 + (rg % 32) * 16 + ((rg / 32) % 4) * 4;
-      else
-        off = rg * static_cast<size_t>(kb) + j0;
-      *reinterpret_cast<uint32_t*>(p.cs + off) = sc[g];
+    for (int g = 0; g < BN / 128; ++g) sc[g] = 0;
+#pragma unroll
+    for (int c = 0; c < BN / 32; c += 2) {
+      uint32_t v[2][32];
+      tmem_ld32(lane_addr + c * 32, v[0]);
+      tmem_ld32(lane_addr + (c + 1) * 32, v[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (p.cq) {
+          uint32_t cr[8];
+          const uint32_t s8 = mx_block32(v[h], p.mx_fmt, p.mx_ceil, cr);
+          sc[(c + h) >> 2] |= s8 << (8 * ((c + h) & 3));
+          uint4* d = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0 + (c + h) * 32);
+          d[0] = make_uint4(cr[0], cr[1], cr[2], cr[3]);
+          d[1] = make_uint4(cr[4], cr[5], cr[6], cr[7]);
+        }
+        if (p.cqT) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[h][j];
+          __syncwarp();
+          uint32_t cc[8];
+          const uint32_t sT = mx_block32_col(xs, lane, p.mx_fmt, p.mx_ceil, cc);
+          __syncwarp();
+          const size_t n = static_cast<size_t>(n0 + (c + h) * 32 + lane);
+          uint4* dT = reinterpret_cast<uint4*>(p.cqT + n * static_cast<size_t>(p.M) + rT);
+          dT[0] = make_uint4(cc[0], cc[1], cc[2], cc[3]);
+          dT[1] = make_uint4(cc[4], cc[5], cc[6], cc[7]);
+          const size_t kbT = static_cast<size_t>(p.M / 32), jT = rT / 32;
+          const size_t offT = p.mx_sf_mma
+                                  ? ((n / 128) * (kbT / 4) + jT / 4) * 512 + (n % 32) * 16 + ((n / 32) % 4) * 4 + jT % 4
+                                  : n * kbT + jT;
+          p.csT[offT] = static_cast<uint8_t>(sT);
+        }
+      }
     }
+    tc_fence_before();
+    __syncwarp();
+    release();
+    if (p.cq) store_row_scales<BN>(p, rg, n0, sc);
     return;
   }
   // float32 output: chunk by chunk
@@ -422,10 +512,10 @@ struct Cfg {
   static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
-  static constexpr int SMEM = STAGES * (STAGE_BYTES + SFA_BYTES + SFB_BYTES) + 2 * STG_BYTES + 256 + 1024;
+  static constexpr int SMEM = STAGES * (STAGE_BYTES + SFA_BYTES + SFB_BYTES) + OUT_BYTES + 256 + 1024;
 };
 
-template <int KIND, int BN>
+template <int KIND, int BN, int MXOUT>
 __global__ void __launch_bounds__(THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_c, const Params p) {
@@ -436,8 +526,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   uint8_t* sB = sA + STAGES * C::A_BYTES;                      // STAGES x B_BYTES
   uint8_t* sSFA = sB + STAGES * C::B_BYTES;                    // STAGES x SFA_BYTES
   uint8_t* sSFB = sSFA + STAGES * C::SFA_BYTES;                // STAGES x SFB_BYTES
-  uint8_t* sOut = sSFB + STAGES * C::SFB_BYTES;                // 2 x STG_BYTES (1024-aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 2 * STG_BYTES);
+  uint8_t* sOut = sSFB + STAGES * C::SFB_BYTES;                // OUT_BYTES (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
@@ -573,7 +663,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<BN, C::KIND == KIND_F8>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, tp.b * p.M + tp.m0,
+      store_tile<BN, C::KIND == KIND_F8, MXOUT>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, tp.b * p.M + tp.m0,
                                          tp.n0, [&] {
                                            if (lane == 0) mbar_arrive(smem_u32(acc_empty));
                                          });
@@ -617,11 +707,11 @@ struct PairCfg {
   // while the MMAs fill the other
   static constexpr int NACC = SCALED ? 1 : 2;
   static_assert(NACC * BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
-  static constexpr int SMEM = STAGES * TX_CTA + 2 * STG_BYTES + 256 + 1024;
+  static constexpr int SMEM = STAGES * TX_CTA + OUT_BYTES + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int KIND>
+template <int KIND, int MXOUT>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
@@ -634,8 +724,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   uint8_t* sB = sA + STAGES_P * C::A_BYTES;                    // STAGES x B_BYTES
   uint8_t* sSFA = sB + STAGES_P * C::B_BYTES;                  // STAGES x SFA_BYTES
   uint8_t* sSFB = sSFA + STAGES_P * C::SFA_BYTES;              // STAGES x SFB_BYTES
-  uint8_t* sOut = sSFB + STAGES_P * C::SFB_BYTES;              // 2 x STG_BYTES (1024-aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 2 * STG_BYTES);
+  uint8_t* sOut = sSFB + STAGES_P * C::SFB_BYTES;              // OUT_BYTES (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);
   uint64_t* full = bars;                                       // used in rank 0
   uint64_t* empty = bars + STAGES_P;
   uint64_t* acc_full = bars + 2 * STAGES_P;
@@ -818,7 +908,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<C::BN, C::KIND == KIND_F8>(p, alpha, tmem + ab * C::BN, q, lane, leader, buf, sOut, &map_c, m0,
+      store_tile<C::BN, C::KIND == KIND_F8, MXOUT>(p, alpha, tmem + ab * C::BN, q, lane, leader, buf, sOut, &map_c, m0,
                                             tp.n0, [&] {
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(acce(ab)));
@@ -863,6 +953,8 @@ struct GemmArgs {
   const void* bias;
   uint8_t* cq;
   uint8_t* cs;
+  uint8_t* cqT;
+  uint8_t* csT;
   int mx_fmt, mx_ceil, mx_sf_mma;
 };
 
@@ -885,6 +977,8 @@ Params make_params(const GemmArgs& g, int tm, int tn, int64_t kbytes) {
   p.bias = static_cast<const __nv_bfloat16*>(g.bias);
   p.cq = g.cq;
   p.cs = g.cs;
+  p.cqT = g.cqT;
+  p.csT = g.csT;
   p.mx_fmt = g.mx_fmt;
   p.mx_ceil = g.mx_ceil;
   p.mx_sf_mma = g.mx_sf_mma;
@@ -908,7 +1002,7 @@ bool encode_c(CUtensorMap* mc, const GemmArgs& g) {
                    CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int MXOUT>
 int launch(const GemmArgs& g, cudaStream_t st) {
   using namespace mxq::gemm;
   using Cf = Cfg<KIND, BN>;
@@ -923,7 +1017,7 @@ int launch(const GemmArgs& g, cudaStream_t st) {
   if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
   Params p = make_params(g, BM, BN, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
-  auto kern = mx_gemm_kernel<KIND, BN>;
+  auto kern = mx_gemm_kernel<KIND, BN, MXOUT>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -938,7 +1032,7 @@ int launch(const GemmArgs& g, cudaStream_t st) {
 
 // Co-resident clusters of two for the pair kernel (cached per device and
 // kernel); 0 if the device cannot hold one.
-template <int KIND>
+template <int KIND, int MXOUT>
 int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
               int smem) {
   static int cache[64] = {};
@@ -970,7 +1064,7 @@ int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, C
   return n > 0 ? n : 0;
 }
 
-template <int KIND>
+template <int KIND, int MXOUT>
 int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   using namespace mxq::gemm;
   using Cf = PairCfg<KIND>;
@@ -998,19 +1092,32 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   Params p = make_params(g, 256, 256, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
   const int grid = 2 * std::min(p.ntiles, pairs);
-  return launch_pdl_cluster(mx_gemm_pair_kernel<KIND>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa,
+  return launch_pdl_cluster(mx_gemm_pair_kernel<KIND, MXOUT>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa,
                             msb, mc, p);
 }
 
 // The pair kernel for M and N multiples of 256 (when the device can hold it),
 // else the single-CTA kernel.
+template <int KIND, int MXOUT>
+int dispatch_out(const GemmArgs& g, cudaStream_t st) {
+  if (g.M % 256 == 0 && g.N % 256 == 0) {
+    const int pairs =
+        max_pairs<KIND, MXOUT>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, mxq::gemm::PairCfg<KIND>::SMEM);
+    if (pairs > 0) return launch_pair<KIND, MXOUT>(g, pairs, st);
+  }
+  return (g.N % 256 == 0) ? launch<KIND, 256, MXOUT>(g, st) : launch<KIND, 128, MXOUT>(g, st);
+}
+
+// The MX outputs are separate kernels (row blocks only; with column
+// blocks), so their epilogue registers do not weigh on the bf16 / float32
+// kernel, nor the column pass on the row-only one.
 template <int KIND>
 int dispatch(const GemmArgs& g, cudaStream_t st) {
-  if (g.M % 256 == 0 && g.N % 256 == 0) {
-    const int pairs = max_pairs<KIND>(mxq::gemm::mx_gemm_pair_kernel<KIND>, mxq::gemm::PairCfg<KIND>::SMEM);
-    if (pairs > 0) return launch_pair<KIND>(g, pairs, st);
+  if constexpr (KIND == mxq::gemm::KIND_F8) return dispatch_out<KIND, 0>(g, st);
+  else {
+    if (g.epi != mxq::gemm::EPI_MX) return dispatch_out<KIND, 0>(g, st);
+    return g.cqT ? dispatch_out<KIND, 2>(g, st) : dispatch_out<KIND, 1>(g, st);
   }
-  return (g.N % 256 == 0) ? launch<KIND, 256>(g, st) : launch<KIND, 128>(g, st);
 }
 
 // Element type code of the MMA's instruction descriptor.
@@ -1077,18 +1184,22 @@ extern "C" int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt, co
 
 extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
                                int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, int out_fmt,
-                               int out_scale_mode, int out_sf_layout, uint8_t* c_q, uint8_t* c_s, void* stream) {
+                               int out_scale_mode, int out_sf_layout, uint8_t* c_q, uint8_t* c_s, uint8_t* c_qT,
+                               uint8_t* c_sT, void* stream) {
   GemmArgs g;
   const int rc = check_mx(g, a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout);
   if (rc != MXQ_OK) return rc;
-  if (!c_q || !c_s) return MXQ_ERR_BAD_ARG;
+  if (!c_q != !c_s || !c_qT != !c_sT || (!c_q && !c_qT)) return MXQ_ERR_BAD_ARG;
+  if ((c_q && (!aligned16(c_q) || !aligned16(c_s))) || (c_qT && (!aligned16(c_qT) || !aligned16(c_sT))))
+    return MXQ_ERR_MISALIGNED;
   if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2) return out_fmt == MXQ_E2M1 ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
   if (out_scale_mode != MXQ_SCALE_FLOOR_OCP && out_scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
   if (out_sf_layout != MXQ_SF_CANONICAL && out_sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
-  if (!aligned16(c_q) || !aligned16(c_s)) return MXQ_ERR_MISALIGNED;
   g.epi = mxq::gemm::EPI_MX;
   g.cq = c_q;
   g.cs = c_s;
+  g.cqT = c_qT;
+  g.csT = c_sT;
   g.mx_fmt = out_fmt;
   g.mx_ceil = out_scale_mode == MXQ_SCALE_CEIL;
   g.mx_sf_mma = out_sf_layout == MXQ_SF_MMA;

@@ -100,12 +100,16 @@ def test_argument_checks_need_no_gpu(so):
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 128, 128, 256, 0, FAKE, 0, None) == -4   # canonical scales
 
     mo = so.mxq_gemm_mx_out
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 2, 0, 0, FAKE, FAKE, None) == -4   # E2M1 output
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 2, 0, FAKE, FAKE, None) == -1   # scale mode
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 2, FAKE, FAKE, None) == -1   # scale layout
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, FAKE, None, None) == -1   # no scales
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, ODD, FAKE, None) == -3
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 100, 128, 1, 0, 0, 0, FAKE, FAKE, None) == -2
+    row = (FAKE, FAKE, None, None)
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 2, 0, 0, *row, None) == -4   # E2M1 output
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 2, 0, *row, None) == -1   # scale mode
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 2, *row, None) == -1   # scale layout
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, FAKE, None, None, None, None) == -1
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, None, None, FAKE, None, None) == -1
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, None, None, None, None, None) == -1
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, ODD, FAKE, None, None, None) == -3
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, None, None, FAKE, ODD, None) == -3
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 100, 128, 1, 0, 0, 0, *row, None) == -2
 
     mm = so.mxq_mm_fp8
     assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 2, FAKE, None, FAKE, None) == -4   # E2M1

@@ -37,25 +37,35 @@ def mx_operand(x, fmt):
     return r["q_row"], r["s_row"]
 
 
-def run_mx_out(lib, aq, as_, bq, bs, fmt, out_fmt, mode, layout):
-    cq, cs = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt,
-                                out_fmt=out_fmt, out_scale_mode=mode, out_sf_layout=layout)
-    cq = cq.cpu().numpy()
-    cs = cs.cpu().numpy()
-    if layout == "mma":
-        cs = omx.sf_from_mma(cs.reshape(-1), cq.shape[0], cq.shape[1] // 32)
-    return cq, cs
+def run_mx_out(lib, aq, as_, bq, bs, fmt, out_fmt, mode, layout, orientation="row"):
+    """Codes and canonical scales of the row blocks and of the (transposed)
+    column blocks; None for an orientation not requested."""
+    out = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fmt,
+                             out_fmt=out_fmt, out_scale_mode=mode, out_sf_layout=layout, orientation=orientation)
+    res = []
+    for q, s in (out[0:2], out[2:4]):
+        if q is None:
+            res += [None, None]
+            continue
+        q = q.cpu().numpy()
+        s = s.cpu().numpy()
+        if layout == "mma":
+            s = omx.sf_from_mma(s.reshape(-1), q.shape[0], q.shape[1] // 32)
+        res += [q, s]
+    return res
 
 
 @pytest.mark.parametrize("out_fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("mode", ["floor", "ceil"])
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
 @pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 1024), (128, 384, 256)])
-def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk):
+@pytest.mark.parametrize("orientation", ["row", "col", "dual"])
+def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk, orientation):
     """A = +-2^j per row (exact in E4M3 with the row scale), B = small
     integers: every product and partial sum is exact in float32, so the
     accumulator equals the float64 product and the MX output must equal the
-    oracle's quantization of it, codes and scales."""
+    oracle's quantization of it, codes and scales, for the row blocks and
+    for the transposed column blocks."""
     M, N, K = mnk
     rng = np.random.default_rng(21)
     a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
@@ -64,10 +74,18 @@ def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk):
     bq, bs = mx_operand(b, "e4m3")
     ref = og.reference(aq, as_, bq, bs, F.E4M3)
     assert np.array_equal(ref, a @ b.T)                          # the operands quantize exactly
-    want = omx.quantize(ref, FMTS[out_fmt], omx.ROW, MODES[mode])
-    cq, cs = run_mx_out(lib, aq, as_, bq, bs, "e4m3", out_fmt, mode, layout)
-    assert_bytes_equal(cq, want["q_row"], "codes")
-    assert_bytes_equal(cs, want["s_row"], "scales")
+    want = omx.quantize(ref, FMTS[out_fmt], omx.DUAL, MODES[mode])
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e4m3", out_fmt, mode, layout, orientation)
+    if orientation in ("row", "dual"):
+        assert_bytes_equal(cq, want["q_row"], "codes")
+        assert_bytes_equal(cs, want["s_row"], "scales")
+    else:
+        assert cq is None
+    if orientation in ("col", "dual"):
+        assert_bytes_equal(cqT, want["q_col"], "column-block codes")
+        assert_bytes_equal(csT, want["s_col"], "column-block scales")
+    else:
+        assert cqT is None
 
 
 def e4m3_spacing(y):
@@ -92,7 +110,7 @@ def test_mx_output_random_within_one_step(lib, mnk):
     bq, bs = mx_operand(b, "e4m3")
     ref = og.reference(aq, as_, bq, bs, F.E4M3)
     want = omx.quantize(ref, F.E4M3, omx.ROW, omx.FLOOR)
-    cq, cs = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e4m3", "floor", "canonical")
+    cq, cs, _, _ = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e4m3", "floor", "canonical")
     ek = cs.astype(int) - 127
     eo = want["s_row"].astype(int) - 127
     assert np.max(np.abs(ek - eo)) <= 1
@@ -119,8 +137,8 @@ def test_mx_output_feeds_the_next_gemm(lib):
     aq, as_ = mx_operand(a, "e4m3")
     bq, bs = mx_operand(b, "e4m3")
     wq, ws = mx_operand(w, "e4m3")
-    cq, cs = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), "e4m3",
-                                out_sf_layout="mma")
+    cq, cs, _, _ = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), "e4m3",
+                                      out_sf_layout="mma")
     d = lib.mx_gemm(cq, cs, t(wq), t(omx.sf_to_mma(ws)), "e4m3", torch.float32)
     c_ref = omx.quantize(a @ b.T, F.E4M3, omx.ROW, omx.FLOOR)
     d_ref = og.reference(c_ref["q_row"], c_ref["s_row"], wq, ws, F.E4M3)
