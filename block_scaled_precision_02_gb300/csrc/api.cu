@@ -132,4 +132,4 @@ extern "C" int mxq_test_stall_next_launch(int which) {
   return MXQ_OK;
 }
 
-extern "C" int mxq_version(void) { return 100; }
+extern "C" int mxq_version(void) { return 200; }

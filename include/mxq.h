@@ -1,7 +1,8 @@
 /*
  * mxq.h -- block-scaled (OCP MX) and per-tensor FP8 quantization of bf16
- * tensors, and the block-scaled GEMM that consumes them, on NVIDIA GB300
- * (sm_103a).  C ABI: plain pointers and sizes, int status codes, no
+ * tensors, the block-scaled GEMM that consumes them (bf16, float32 or MX
+ * output; same or mixed 8-bit formats) and the per-tensor FP8 GEMM, on NVIDIA
+ * GB300 (sm_103a).  C ABI: plain pointers and sizes, int status codes, no
  * exceptions.
  *
  * Conventions for every entry point
@@ -30,7 +31,7 @@
  *        dimension).
  *  [FP8] AstrAI astrai/extension/ops/fp8.py (commit 962c10c52b): commit
  *        message (last-block delayed-scaling fold with an atomic ticket) and
- *        the quantize / quantize_dual docstrings.
+ *        the quantize / quantize_dual / mm_fp8 docstrings.
  *  [FAF] "Format-aware fusion for FP4" (theaicronicle.com): MXFP4 with
  *        row-gradient stochastic rounding and a fixed-sign 32-point
  *        Hadamard; producers emit the scale layout their consumer reads.
