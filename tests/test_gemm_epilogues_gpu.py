@@ -212,5 +212,56 @@ def test_mm_fp8_views_fold_and_bad_layouts_raise(lib):
         lib.mm_fp8(a8, w8, scale, trans_a=True, trans_b=True)   # op(a) M-contiguous
 
 
+# ---------------------------------------------------------------- full sizes, sampled
+def _rows(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, k, replace=False))
+
+
+def test_full_size_mx_output_sampled(lib):
+    """8192 x 4096 activations times 4096 x 4096 weights (MXFP8 E4M3), as the
+    bench runs it, with row and column-block E4M3 outputs: sampled output
+    rows and output columns against the oracle's MX quantization of the
+    float64 product (the property bar of the random test)."""
+    M, N, K = 8192, 4096, 4096
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e4m3", "floor", "mma", "dual")
+    rows = _rows(M, 16, 1)
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E4M3, rows, np.arange(N))
+    want = omx.quantize(ref, F.E4M3, omx.ROW, omx.FLOOR)
+    assert np.max(np.abs(cs[rows].astype(int) - want["s_row"].astype(int))) <= 1
+    assert np.mean(cq[rows] == want["q_row"]) >= 0.99
+    # column blocks: 32-row groups of sampled output columns
+    cols = _rows(N, 8, 2)
+    groups = _rows(M // 32, 8, 3)
+    rr = (groups[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+    refc = og.reference_rows_cols(aq, as_, bq, bs, F.E4M3, rr, cols)          # [8*32][8]
+    wantc = omx.quantize(refc.T.reshape(len(cols), len(groups), 32).reshape(len(cols), -1), F.E4M3, omx.ROW,
+                         omx.FLOOR)
+    got_codes = cqT[cols][:, rr]
+    got_scales = csT[cols][:, groups]
+    assert np.max(np.abs(got_scales.astype(int) - wantc["s_row"].astype(int))) <= 1
+    assert np.mean(got_codes == wantc["q_row"]) >= 0.99
+
+
+def test_full_size_mm_fp8_sampled(lib):
+    """The bench's per-tensor FP8 product at full size and launch
+    configuration: 8192 x 4096 E4M3 operand times the transposed view of a
+    4096 x 4096 one, with bias; sampled rows and columns within the gate."""
+    M, N, K = 8192, 4096, 4096
+    rng = np.random.default_rng(27)
+    # seeded finite E4M3 codes (every code but the NaN patterns 0x7F / 0xFF)
+    x8n = (rng.integers(0, 0x7F, (M, K), dtype=np.uint8) | (rng.integers(0, 2, (M, K), dtype=np.uint8) << 7))
+    w8n = (rng.integers(0, 0x7F, (N, K), dtype=np.uint8) | (rng.integers(0, 2, (N, K), dtype=np.uint8) << 7))
+    bias = inputs.weights(1, N, seed=9).reshape(N)
+    sc = torch.tensor([0.75], dtype=torch.float32, device=dev)
+    c = lib.mm_fp8(t(x8n), t(w8n), sc, trans_b=True, bias=bias.to(dev), fmt="e4m3").float().cpu().numpy()
+    rows, cols = _rows(M, 64, 4), _rows(N, 64, 5)
+    ref = og.mm_fp8_reference(x8n[rows], w8n[cols], F.E4M3, 0.75, f64(bias)[cols])
+    assert og.gate_error(c[np.ix_(rows, cols)].astype(np.float64), ref) <= 2e-3
+
+
 def test_device_status_clean_after_epilogues(lib):
     assert lib.last_device_status() == 0

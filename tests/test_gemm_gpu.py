@@ -163,6 +163,22 @@ def test_full_size_ffn_sampled(lib):
              lambda n, k: inputs.weights(n, k, seed=5))
 
 
+def test_full_size_mixed_sampled(lib):
+    """The bench's mixed-format product: the 8192 x 4096 E5M2 gradient times
+    the 4096 x 4096 E4M3 weights."""
+    M, N, K = 8192, 4096, 4096
+    a = f64(inputs.gradients(M, K, seed=1))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = oracle_operand(a, "e5m2")
+    bq, bs = oracle_operand(b, "e4m3")
+    got = gpu_gemm(lib, aq, as_, bq, bs, "e5m2", b_fmt="e4m3")
+    rng = np.random.default_rng(8)
+    rows = np.sort(rng.choice(M, 64, replace=False))
+    cols = np.sort(rng.choice(N, 64, replace=False))
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E5M2, rows, cols, F.E4M3)
+    assert og.gate_error(got[np.ix_(rows, cols)], ref) <= TOL
+
+
 def test_full_size_fp4_sampled(lib):
     """4096 x 14336 gradient times 4096 x 14336 operand (MXFP4 E2M1)."""
     _sampled(lib, 4096, 4096, 14336, "e2m1", lambda m, k: inputs.heavy_gradient(m, k, seed=6),
