@@ -318,6 +318,11 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
     for _ in range(3):
         fp4q4()
     ms_q5b = timed(fp4q4, args.steps)
+    # ceil scales (the recipe runs both scale rules)
+    fp4qc = lambda: q(G5, "e2m1", "ceil", "row", rounding="sr", hadamard32=True, sr_key=0, hadamard_seed=7)
+    for _ in range(3):
+        fp4qc()
+    ms_q5c = timed(fp4qc, args.steps)
     b5 = q(B5, "e2m1", "floor", "row", hadamard32=True, hadamard_seed=7)
     fn5 = lambda: mxq.mx_gemm(g5[0], g5[1], b5[0], b5[1], "e2m1")
     for _ in range(3):
@@ -331,7 +336,7 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
                                    "peak_source": f"bf16 burst x {RATIO['e2m1']} ({peak_src})",
                                    "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"),
                                                           "mxfp4_4096x4096x14336")}})
-    return (ms_q5, ms_q5b), 3 * args.steps
+    return (ms_q5, ms_q5b, ms_q5c), 4 * args.steps
 
 
 def pertensor_part(args, mxq, X, timed):
@@ -347,7 +352,14 @@ def pertensor_part(args, mxq, X, timed):
     for _ in range(3):
         pt()
     k = max(16, args.steps)
-    return timed(pt, k), k
+    ms_dual = timed(pt, k)
+
+    def ptt():                              # transposed output only (x8T), same ring
+        mxq.quantize(X3, ring[17:18], "e4m3", True, ring, t3["k"] % 16)
+        t3["k"] += 1
+    for _ in range(3):
+        ptt()
+    return (ms_dual, timed(ptt, k)), 2 * k
 
 
 def small_part(args, mxq, X, timed):
@@ -629,10 +641,13 @@ def run_ours(args, rank, world):
         "gpu_launches_detail": launch_detail,
         "gemm": {"metric": "MX GEMM TFLOP/s", "rows": gemm_rows, "cpu_baseline": gcpu},
         "rows": {
-            "pertensor_fp8_ring_4096x14336_dual": hbm_row(b3, ms3, hbm),
+            "pertensor_fp8_ring_4096x14336_dual": hbm_row(b3, ms3[0], hbm),
+            "pertensor_fp8_ring_4096x14336_transposed": hbm_row(pertensor_bytes(4096, 14336, "col"), ms3[1], hbm),
             "mxfp4_hadamard_sr_quantize_4096x14336": dict(hbm_row(
                 b_q5, ms_q5[0], hbm, "one Philox-4x32-10 draw per element: integer-ALU bound"),
                 alu_roofline=alu_roofline("sr_hadamard_e2m1_4096x14336", 4096 * 14336, ms_q5[0], sm_max)),
+            "mxfp4_hadamard_sr_ceil_quantize_4096x14336": hbm_row(
+                b_q5, ms_q5[2], hbm, "ceil scales; one Philox-4x32-10 draw per element"),
             "mxfp4_hadamard_sr4_quantize_4096x14336": dict(hbm_row(
                 b_q5, ms_q5[1], hbm, "option SR4: four draws per Philox-4x32-10 call"),
                 alu_roofline=alu_roofline("sr4_hadamard_e2m1_4096x14336", 4096 * 14336, ms_q5[1], sm_max)),
