@@ -101,20 +101,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
-// Cluster-scope variants, for barriers that other CTAs of the cluster (or
+// Cluster-scope variant, for barriers that other CTAs of the cluster (or
 // their async copies and tensor-core commits) complete.
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
@@ -127,28 +115,9 @@ __device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint32_t bar, uint32_t pa
   return ok != 0;
 }
 
-// Bounded wait with cluster-scope acquire (same limit and policy as mbar_wait).
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, int* status) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      const unsigned long long dt = globaltimer_ns() - t0;
-      if (dt > kWaitLimitNs) {
-        record_timeout(status);
-        return false;
-      }
-      if (dt > 4000u) {
-        if (mbar_try_wait_cl_sleep(bar, parity, 20000u)) return true;
-      }
-    }
-  }
-}
-
 // Bounded wait that lets the hardware suspend the thread until the phase
-// completes (no polling loop competing for issue slots and the barrier unit);
-// for waits off the latency-critical path.  Cluster-scope acquire.
+// completes (no polling loop competing for issue slots and the barrier unit
+// with the thread that issues tensor-core work); cluster-scope acquire.
 __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, int* status) {
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
