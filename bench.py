@@ -244,9 +244,10 @@ def oracle_gemm_baseline(budget_s: float = 6.0):
 # ---------------------------------------------------------------- measured rows besides the headline
 def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     """MXFP8 GEMMs 8192x4096x4096 and 8192x14336x4096 on operands from our
-    quantizer (A = the activation quantized by the headline step), and the
-    mixed-format product of the headline's E5M2 gradient with the E4M3
-    weights."""
+    quantizer (A = the activation quantized by the headline step), the
+    mixed-format products of the headline's E5M2 gradient with the E4M3
+    weights and of the activation with E2M1 weights, the MX-output and
+    per-tensor products."""
     aq, as_, _, _ = outs[0]
     M, K = 8192, 4096
     W, W2 = X["W"], X["W2"]
@@ -270,6 +271,12 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
                                        "unit": "TFLOP/s", "frac": round(tf / pk, 4),
                                        "peak_source": f"bf16 burst x {RATIO['e4m3']} ({peak_src})",
                                        "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"), name)}})
+    # MXFP8 activations times MXFP4 weights (the weights quantized to E2M1 by
+    # our quantizer; the E2M1 codes are widened on their way into shared memory)
+    w4q, w4s, _, _ = q(W, "e2m1", "floor", "row")
+    fn = lambda: mxq.mx_gemm(aq, as_, w4q, w4s, "e4m3", b_fmt="e2m1")
+    n += extra_gemm_row(args, fn, timed, "mxfp8_x_mxfp4_e4m3_x_e2m1_8192x4096x4096", M, 4096, K, bf16, peak_src,
+                        gemm_rows)
     # the same MXFP8 product written as MX E4M3 codes + scales (MMA layout:
     # the next GEMM's A operand) straight from the accumulator
     fn = lambda: mxq.mx_gemm_mx_out(aq, as_, wq, ws, "e4m3", out_fmt="e4m3", out_sf_layout="mma")

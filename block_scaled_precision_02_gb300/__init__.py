@@ -197,8 +197,8 @@ def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.
             out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None, b_fmt=None) -> torch.Tensor:
     """C = A * B^T from MX operands (A [M][K], B [N][K] codes, scales in the
     MMA layout).  ``fmt`` is A's element format and B's unless ``b_fmt`` is
-    given (E4M3 and E5M2 mix; E2M1 pairs with E2M1).  Returns bf16 (or
-    float32) [M][N]."""
+    given (any two of E4M3, E5M2 and E2M1: an E2M1 operand beside an 8-bit
+    one runs at the 8-bit rate).  Returns bf16 (or float32) [M][N]."""
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
     M = a_q.shape[0]

@@ -87,6 +87,7 @@ struct Params {
   int mx_fmt, mx_ceil, mx_sf_mma;
   int* status;
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
+  uint32_t tx_bytes;  // bytes the loads of one stage complete on its "full" barrier (both CTAs of a pair)
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
 
@@ -503,7 +504,6 @@ struct Cfg {
   static constexpr int SFA_BYTES = 512 * SF_CHUNKS;
   static constexpr int SFB_BYTES = 512 * SF_CHUNKS * (BN / 128);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int TX_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   // tensor memory: accumulator BN columns, then per stage the scale chunks:
   // A (4 columns per chunk), then B (per chunk, BN / 32 consecutive columns:
   // column j holds rows 32 j .. 32 j + 31 of the tile)
@@ -576,7 +576,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           if (!mbar_wait(smem_u32(&empty[s]), ((u / STAGES) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, C::TX_BYTES);
+          mbar_arrive_expect_tx(fb, p.tx_bytes);
           tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
           tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
           if constexpr (C::SCALED) {
@@ -698,7 +698,7 @@ struct PairCfg {
   static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
   static constexpr int SFA_BYTES = 512 * SF_CHUNKS;
   static constexpr int SFB_BYTES = 2 * SFA_BYTES;       // both 128-row halves of B
-  static constexpr int TX_CTA = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int TX_CTA = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // shared memory per stage
   static constexpr int SFA_COLS = 4 * SF_CHUNKS;
   static constexpr int SFB_COLS = 8 * SF_CHUNKS;
   static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
@@ -792,7 +792,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           if (!mbar_wait_suspend(smem_u32(&empty[s]), ((u / STAGES_P) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (rank == 0 && blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = cluster_map(smem_u32(&full[s]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::TX_CTA);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), p.tx_bytes);
           tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
           tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
           if constexpr (C::SCALED) {
@@ -947,6 +947,8 @@ struct GemmArgs {
   int64_t batch, M, N, K;
   int a_batched, b_batched;
   uint32_t a_type, b_type;
+  int fp4;                        // both operands packed E2M1: kind::mxf4
+  int a_u4, b_u4;                 // packed E2M1 beside an 8-bit operand (see encode_operand)
   int epi;
   void* c;                        // EPI_BF16 / EPI_FP32 output [batch * M][N]
   const float* alpha;
@@ -1002,6 +1004,29 @@ bool encode_c(CUtensorMap* mc, const GemmArgs& g) {
                    CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// An operand's code map: 128-byte K steps of `box_rows` rows, 128-byte
+// swizzle.  Codes are bytes (8-bit formats, or packed E2M1 for kind::mxf4,
+// kbytes = K / 2).  Packed E2M1 beside an 8-bit operand (kind::mxf8f6f4)
+// goes through the 16 x 4-bit type that widens every 8 packed bytes to a
+// 16-byte slot: a K step is then 128 elements in the same 128 bytes of
+// shared memory per row as an 8-bit operand, the layout the tensor core
+// reads for 4-bit elements of that kind, and the map's x coordinate counts
+// elements, so the kernels' coordinates (kb * 128) are unchanged.
+bool encode_operand(CUtensorMap* m, const void* q, bool u4, int64_t K, int64_t kbytes, uint64_t rows,
+                    uint32_t box_rows) {
+  using namespace mxq::gemm;
+  if (u4)
+    return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, q, K, rows, K / 2, 128, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, kbytes, rows, kbytes, BKB, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Transaction bytes of one operand tile: the widened E2M1 load completes the
+// packed bytes it reads (half its shared-memory footprint; the padding
+// slots are not written).
+constexpr uint32_t tx_bytes(int smem_bytes, bool u4) { return static_cast<uint32_t>(u4 ? smem_bytes / 2 : smem_bytes); }
+
 template <int KIND, int BN, int MXOUT>
 int launch(const GemmArgs& g, cudaStream_t st) {
   using namespace mxq::gemm;
@@ -1010,13 +1035,12 @@ int launch(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap ma, mb, mc;
   const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
   const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
-  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_q, kbytes, arows, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
-  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_q, kbytes, brows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
+  if (!encode_operand(&ma, g.a_q, g.a_u4, g.K, kbytes, arows, BM)) return MXQ_ERR_CUDA;
+  if (!encode_operand(&mb, g.b_q, g.b_u4, g.K, kbytes, brows, BN)) return MXQ_ERR_CUDA;
   if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
   Params p = make_params(g, BM, BN, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
+  p.tx_bytes = tx_bytes(Cf::A_BYTES, g.a_u4) + tx_bytes(Cf::B_BYTES, g.b_u4) + Cf::SFA_BYTES + Cf::SFB_BYTES;
   auto kern = mx_gemm_kernel<KIND, BN, MXOUT>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -1073,10 +1097,8 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   CUtensorMap ma, mb, msa, msb, mc;
   const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
   const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
-  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_q, kbytes, arows, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
-  if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_q, kbytes, brows, kbytes, BKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXQ_ERR_CUDA;
+  if (!encode_operand(&ma, g.a_q, g.a_u4, g.K, kbytes, arows, BM)) return MXQ_ERR_CUDA;
+  if (!encode_operand(&mb, g.b_q, g.b_u4, g.K, kbytes, brows, 128)) return MXQ_ERR_CUDA;
   msa = CUtensorMap{};
   msb = CUtensorMap{};
   if (Cf::SCALED) {
@@ -1091,6 +1113,7 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
   Params p = make_params(g, 256, 256, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
+  p.tx_bytes = 2 * (tx_bytes(Cf::A_BYTES, g.a_u4) + tx_bytes(Cf::B_BYTES, g.b_u4) + Cf::SFA_BYTES + Cf::SFB_BYTES);
   const int grid = 2 * std::min(p.ntiles, pairs);
   return launch_pdl_cluster(mx_gemm_pair_kernel<KIND, MXOUT>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa,
                             msb, mc, p);
@@ -1120,8 +1143,14 @@ int dispatch(const GemmArgs& g, cudaStream_t st) {
   }
 }
 
-// Element type code of the MMA's instruction descriptor.
-uint32_t mma_type(int fmt) { return fmt == MXQ_E4M3 ? 0u : 1u; }   // E5M2: 1 (mxf8f6f4 / f8f6f4); E2M1: 1 (mxf4)
+// Element type code of the MMA's instruction descriptor: E4M3 0 and E5M2 1
+// (kind::mxf8f6f4 / f8f6f4); E2M1 1 in kind::mxf4 and 5 in kind::mxf8f6f4.
+uint32_t mma_type(int fmt, bool kind_mxf4) {
+  if (fmt == MXQ_E2M1) return kind_mxf4 ? 1u : 5u;
+  return fmt == MXQ_E4M3 ? 0u : 1u;
+}
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E5M2 || f == MXQ_E2M1; }
 
@@ -1130,13 +1159,16 @@ int check_mx(GemmArgs& g, const void* a_q, const uint8_t* a_s, int a_fmt, const 
              int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout) {
   if (!a_q || !a_s || !b_q || !b_s) return MXQ_ERR_BAD_ARG;
   if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return MXQ_ERR_BAD_ARG;
-  // E2M1 pairs only with E2M1 (kind::mxf4 takes packed FP4 for both operands)
-  if ((a_fmt == MXQ_E2M1) != (b_fmt == MXQ_E2M1)) return MXQ_ERR_UNSUPPORTED;
   if (sf_layout != MXQ_SF_MMA) return sf_layout == MXQ_SF_CANONICAL ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
-  const bool fp4 = a_fmt == MXQ_E2M1;
+  // Both E2M1: kind::mxf4 on packed operands.  One E2M1 beside an 8-bit
+  // operand: kind::mxf8f6f4, the E2M1 codes widened on their way into
+  // shared memory (encode_operand), which wants 32-byte aligned rows.
+  const bool fp4 = a_fmt == MXQ_E2M1 && b_fmt == MXQ_E2M1;
+  const bool a_u4 = a_fmt == MXQ_E2M1 && !fp4, b_u4 = b_fmt == MXQ_E2M1 && !fp4;
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % (fp4 ? 256 : 128)) return MXQ_ERR_BAD_SHAPE;
   if (M > (1ll << 31) - 256 || N > (1ll << 31) - 256 || K > (1ll << 31) - 256) return MXQ_ERR_BAD_SHAPE;
   if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_s) || !aligned16(b_s)) return MXQ_ERR_MISALIGNED;
+  if ((a_u4 && !aligned32(a_q)) || (b_u4 && !aligned32(b_q))) return MXQ_ERR_MISALIGNED;
   g = GemmArgs{};
   g.a_q = a_q;
   g.a_s = a_s;
@@ -1146,15 +1178,18 @@ int check_mx(GemmArgs& g, const void* a_q, const uint8_t* a_s, int a_fmt, const 
   g.M = M;
   g.N = N;
   g.K = K;
-  g.a_type = mma_type(a_fmt);
-  g.b_type = mma_type(b_fmt);
+  g.a_type = mma_type(a_fmt, fp4);
+  g.b_type = mma_type(b_fmt, fp4);
+  g.fp4 = fp4;
+  g.a_u4 = a_u4;
+  g.b_u4 = b_u4;
   return MXQ_OK;
 }
 
-int run_mx(const GemmArgs& g, bool fp4, void* stream) {
+int run_mx(const GemmArgs& g, void* stream) {
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
   auto st = static_cast<cudaStream_t>(stream);
-  return fp4 ? dispatch<mxq::gemm::KIND_MXF4>(g, st) : dispatch<mxq::gemm::KIND_MXF8>(g, st);
+  return g.fp4 ? dispatch<mxq::gemm::KIND_MXF4>(g, st) : dispatch<mxq::gemm::KIND_MXF8>(g, st);
 }
 
 int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s, int b_fmt,
@@ -1166,7 +1201,7 @@ int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q
   if (!aligned16(c)) return MXQ_ERR_MISALIGNED;
   g.c = c;
   g.epi = out_fp32 ? mxq::gemm::EPI_FP32 : mxq::gemm::EPI_BF16;
-  return run_mx(g, a_fmt == MXQ_E2M1, stream);
+  return run_mx(g, stream);
 }
 
 }  // namespace
@@ -1203,7 +1238,7 @@ extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, c
   g.mx_fmt = out_fmt;
   g.mx_ceil = out_scale_mode == MXQ_SCALE_CEIL;
   g.mx_sf_mma = out_sf_layout == MXQ_SF_MMA;
-  return run_mx(g, a_fmt == MXQ_E2M1, stream);
+  return run_mx(g, stream);
 }
 
 extern "C" int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M, int64_t N, int64_t K,
@@ -1228,8 +1263,8 @@ extern "C" int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M
   g.K = K;
   g.a_batched = batch > 1 ? a_batched : 0;
   g.b_batched = batch > 1 ? b_batched : 0;
-  g.a_type = mma_type(fmt);
-  g.b_type = mma_type(fmt);
+  g.a_type = mma_type(fmt, false);
+  g.b_type = mma_type(fmt, false);
   g.epi = mxq::gemm::EPI_BF16;
   g.c = c;
   g.alpha = scale;

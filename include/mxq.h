@@ -176,9 +176,11 @@ int mxq_gemm(const void* a_q, const uint8_t* a_s, const void* b_q,
 /* ---- mixed-format block-scaled GEMM (same product; [MX] FP8 section: E4M3
  * for precision beside E5M2 for range, e.g. an E5M2 gradient times an E4M3
  * operand) ----------------------------------------------------------------------
- * As mxq_gemm, with a_fmt for A and b_fmt for B: any of E4M3 / E5M2 with
- * either, or E2M1 with E2M1.  E2M1 beside an 8-bit format returns
- * MXQ_ERR_UNSUPPORTED. */
+ * As mxq_gemm, with a_fmt for A and b_fmt for B: any pair of E4M3 / E5M2 /
+ * E2M1, e.g. MXFP8 activations times MXFP4 weights.  E2M1 with E2M1 is
+ * mxq_gemm's MXFP4 product (K % 256 == 0).  E2M1 beside an 8-bit format
+ * runs at the 8-bit rate and needs K % 128 == 0 and the E2M1 codes (still
+ * packed [rows][K/2] in memory) 32-byte aligned, else MXQ_ERR_MISALIGNED. */
 int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt,
                    const void* b_q, const uint8_t* b_s, int b_fmt,
                    int64_t M, int64_t N, int64_t K, int sf_layout, void* c,

@@ -51,6 +51,7 @@ def test_strerror_and_version(so):
 
 FAKE = ctypes.c_void_p(0x10000)           # 16-byte aligned, never dereferenced
 ODD = ctypes.c_void_p(0x10008)
+FAKE16 = ctypes.c_void_p(0x10010)         # 16-byte but not 32-byte aligned
 
 
 def test_argument_checks_need_no_gpu(so):
@@ -93,8 +94,14 @@ def test_argument_checks_need_no_gpu(so):
     assert g(ODD, FAKE, FAKE, FAKE, 128, 128, 128, 0, 1, FAKE, 0, None) == -3
 
     mg = so.mxq_gemm_mixed
-    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 2, 128, 128, 256, 1, FAKE, 0, None) == -4   # E4M3 x E2M1
-    assert mg(FAKE, FAKE, 2, FAKE, FAKE, 1, 128, 128, 256, 1, FAKE, 0, None) == -4   # E2M1 x E5M2
+    # E2M1 beside an 8-bit operand: K % 128 as for 8-bit pairs, and the E2M1
+    # codes 32-byte aligned (a 16-byte aligned pointer is enough for the other)
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 2, 128, 128, 192, 1, FAKE, 0, None) == -2   # E4M3 x E2M1
+    assert mg(FAKE, FAKE, 0, FAKE, FAKE, 2, 128, 128, 128, 1, None, 0, None) == -1   # shape passed; no C
+    assert mg(FAKE, FAKE, 0, FAKE16, FAKE, 2, 128, 128, 256, 1, FAKE, 0, None) == -3
+    assert mg(FAKE16, FAKE, 2, FAKE, FAKE, 1, 128, 128, 256, 1, FAKE, 0, None) == -3   # E2M1 x E5M2
+    assert mg(FAKE16, FAKE, 0, FAKE, FAKE, 2, 128, 128, 256, 1, None, 0, None) == -1   # alignment passed
+    assert mg(FAKE, FAKE, 2, FAKE, FAKE, 2, 128, 128, 128, 1, FAKE, 0, None) == -2   # E2M1 x E2M1: K % 256
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 5, 128, 128, 256, 1, FAKE, 0, None) == -1   # unknown format
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 100, 128, 256, 1, FAKE, 0, None) == -2
     assert mg(FAKE, FAKE, 0, FAKE, FAKE, 1, 128, 128, 256, 0, FAKE, 0, None) == -4   # canonical scales

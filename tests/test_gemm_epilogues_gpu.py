@@ -88,6 +88,34 @@ def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk, or
         assert cqT is None
 
 
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e2m1"), ("e2m1", "e4m3")])
+@pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 384)])
+def test_mx_output_exact_fp8_x_fp4(lib, fa, fb, mnk):
+    """The MX output of a mixed MXFP8 x MXFP4 product: A = +-2^j per row and
+    B = integers in [-4, 4] are exact in E4M3 and in E2M1 alike, every sum is
+    exact in float32, so the row and column blocks must equal the oracle's
+    quantization of the float64 product bit for bit."""
+    M, N, K = mnk
+    rng = np.random.default_rng(23)
+    a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
+    b = rng.integers(-4, 5, (N, K)).astype(np.float64)
+    fmts = {"e4m3": F.E4M3, "e2m1": F.E2M1}
+    ra = omx.quantize(a, fmts[fa], omx.ROW, omx.FLOOR)
+    rb = omx.quantize(b, fmts[fb], omx.ROW, omx.FLOOR)
+    aq, as_, bq, bs = ra["q_row"], ra["s_row"], rb["q_row"], rb["s_row"]
+    ref = og.reference(aq, as_, bq, bs, fmts[fa], fmts[fb])
+    assert np.array_equal(ref, a @ b.T)                          # the operands quantize exactly
+    want = omx.quantize(ref, F.E4M3, omx.DUAL, omx.FLOOR)
+    out = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), fa, b_fmt=fb,
+                             out_fmt="e4m3", out_scale_mode="floor", out_sf_layout="canonical",
+                             orientation="dual")
+    cq, cs, cqT, csT = (x.cpu().numpy() for x in out)
+    assert_bytes_equal(cq, want["q_row"], "codes")
+    assert_bytes_equal(cs, want["s_row"], "scales")
+    assert_bytes_equal(cqT, want["q_col"], "column-block codes")
+    assert_bytes_equal(csT, want["s_col"], "column-block scales")
+
+
 def e4m3_spacing(y):
     """Grid spacing of E4M3 at magnitude y (3 mantissa bits; subnormal step 2^-9)."""
     a = np.abs(y)

@@ -110,6 +110,55 @@ def test_mixed_formats_gate(lib, fa, fb, mnk):
     assert og.gate_error(got, ref) <= TOL, (og.gate_error(got, ref), og.frobenius_rel(got, ref))
 
 
+MIXED_FP4 = [("e4m3", "e2m1"), ("e5m2", "e2m1"), ("e2m1", "e4m3")]
+
+
+@pytest.mark.parametrize("fa,fb", MIXED_FP4)
+@pytest.mark.parametrize("mn", [(128, 256), (256, 512), (128, 128)])
+def test_fp8_x_fp4_unit_rows_exactly(lib, fa, fb, mn):
+    """An 8-bit operand beside a packed E2M1 one (kind::mxf8f6f4 with the
+    E2M1 codes widened in shared memory): B's unit rows make C[:, n] a
+    scaled copy of one dequantized A column, exact in bf16, so the widened
+    layout, both element types and both operands' scales are checked bit for
+    bit on the single-CTA kernel (M = 128) and the CTA pair."""
+    rng = np.random.default_rng(5)
+    M, N = mn
+    K = 512
+    a = rng.standard_normal((M, K)) * np.exp2(rng.integers(-6, 6, size=(M, K // 32))).repeat(32, 1)
+    aq, as_ = oracle_operand(a, fa)
+    perm = rng.permutation(K)[:N]
+    b = np.zeros((N, K))
+    b[np.arange(N), perm] = np.exp2(rng.integers(-3, 4, size=N)) * 1.5
+    bq, bs = oracle_operand(b, fb)
+    ref = og.reference(aq, as_, bq, bs, FMTS[fa], FMTS[fb])
+    got = gpu_gemm(lib, aq, as_, bq, bs, fa, b_fmt=fb)
+    assert np.array_equal(got, ref), f"max abs diff {np.max(np.abs(got - ref))}"
+
+
+def _mixed_input(fmt, rows, K, seed):
+    if fmt == "e2m1":
+        return f64(inputs.fp4_operand(rows, K, seed=seed))
+    if fmt == "e5m2":
+        return f64(inputs.gradients(rows, K, seed=seed))
+    return f64(inputs.activations(rows, K, seed=seed))
+
+
+@pytest.mark.parametrize("fa,fb", MIXED_FP4)
+@pytest.mark.parametrize("mnk", [(256, 512, 1024), (384, 384, 640), (128, 256, 128), (512, 768, 2048)])
+def test_fp8_x_fp4_gate(lib, fa, fb, mnk):
+    """MXFP8 activations (or E5M2 gradients) times MXFP4 weights, and the
+    reverse, against the float64 product of the dequantized operands; K
+    down to one 128-element step and K not a multiple of 256."""
+    M, N, K = mnk
+    a = _mixed_input(fa, M, K, 0)
+    b = _mixed_input(fb, N, K, 4)
+    aq, as_ = oracle_operand(a, fa)
+    bq, bs = oracle_operand(b, fb)
+    ref = og.reference(aq, as_, bq, bs, FMTS[fa], FMTS[fb])
+    got = gpu_gemm(lib, aq, as_, bq, bs, fa, b_fmt=fb)
+    assert og.gate_error(got, ref) <= TOL, (og.gate_error(got, ref), og.frobenius_rel(got, ref))
+
+
 def test_fp32_output_and_many_tiles(lib):
     """float32 epilogue, and more output tiles than SMs (the persistent loop)."""
     M, N, K = 2048, 4096, 256
@@ -176,6 +225,22 @@ def test_full_size_mixed_sampled(lib):
     rows = np.sort(rng.choice(M, 64, replace=False))
     cols = np.sort(rng.choice(N, 64, replace=False))
     ref = og.reference_rows_cols(aq, as_, bq, bs, F.E5M2, rows, cols, F.E4M3)
+    assert og.gate_error(got[np.ix_(rows, cols)], ref) <= TOL
+
+
+def test_full_size_fp8_x_fp4_sampled(lib):
+    """The bench's MXFP8 x MXFP4 product: 8192 x 4096 E4M3 activations times
+    4096 x 4096 E2M1 weights."""
+    M, N, K = 8192, 4096, 4096
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.fp4_operand(N, K, seed=8))
+    aq, as_ = oracle_operand(a, "e4m3")
+    bq, bs = oracle_operand(b, "e2m1")
+    got = gpu_gemm(lib, aq, as_, bq, bs, "e4m3", b_fmt="e2m1")
+    rng = np.random.default_rng(9)
+    rows = np.sort(rng.choice(M, 64, replace=False))
+    cols = np.sort(rng.choice(N, 64, replace=False))
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E4M3, rows, cols, F.E2M1)
     assert og.gate_error(got[np.ix_(rows, cols)], ref) <= TOL
 
 
