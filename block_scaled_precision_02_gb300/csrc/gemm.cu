@@ -683,16 +683,28 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // holds rows m0 + 128 r .. of A, rows n0 + 128 r .. of B, A's scale chunks of
 // its own rows and B's of all 256 rows.  The pair's first CTA (rank 0) owns
 // the stage ring's "full" barriers (both CTAs' loads complete on them), the
-// accumulator-empty barrier (all 8 epilogue warps arrive) and issues the
-// tensor-core work (scale copies from warp 6, MMAs from warp 1); its MMA
-// commits arrive on the "empty" and accumulator-full barriers of both CTAs.
-template <int KIND_>
+// accumulator-empty barrier (all epilogue warps of both CTAs arrive) and
+// issues the tensor-core work (scale copies from warp 6, MMAs from warp 1);
+// its MMA commits arrive on the "empty" and accumulator-full barriers of
+// both CTAs.
+//
+// The MX outputs quantize in the epilogue, which then does far more
+// arithmetic per accumulator value; with one epilogue warp per SM
+// sub-partition that work is latency-bound, so these variants run two groups
+// of four epilogue warps (warps 2-5 and 7-10), each draining 128 of the 256
+// accumulator columns.
+template <int KIND_, int MXOUT_ = 0>
 struct PairCfg {
   static constexpr int KIND = KIND_;
   static constexpr bool FP4 = KIND == KIND_MXF4;
   static constexpr bool SCALED = KIND != KIND_F8;
   static constexpr int BN = 256;                        // columns per tile (both CTAs)
-  static constexpr int STAGES = FP4 ? 5 : 6;
+  static constexpr int EPI_GROUPS = MXOUT_ ? 2 : 1;
+  static constexpr int EPI_COLS = BN / EPI_GROUPS;      // accumulator columns per epilogue group
+  static constexpr int THREADS = PAIR_THREADS + (EPI_GROUPS - 1) * 128;
+  // the column-block output transposes through 32 x 33 words per epilogue warp
+  static constexpr int OUT = MXOUT_ == 2 ? EPI_GROUPS * 4 * 32 * 33 * 4 : OUT_BYTES;
+  static constexpr int STAGES = (FP4 || MXOUT_ == 2) ? 5 : 6;
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
   static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
@@ -707,16 +719,16 @@ struct PairCfg {
   // while the MMAs fill the other
   static constexpr int NACC = SCALED ? 1 : 2;
   static_assert(NACC * BN + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
-  static constexpr int SMEM = STAGES * TX_CTA + OUT_BYTES + 256 + 1024;
+  static constexpr int SMEM = STAGES * TX_CTA + OUT + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 template <int KIND, int MXOUT>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
+__global__ void __launch_bounds__(PairCfg<KIND, MXOUT>::THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
                     const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = PairCfg<KIND>;
+  using C = PairCfg<KIND, MXOUT>;
   constexpr int STAGES_P = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -724,8 +736,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   uint8_t* sB = sA + STAGES_P * C::A_BYTES;                    // STAGES x B_BYTES
   uint8_t* sSFA = sB + STAGES_P * C::B_BYTES;                  // STAGES x SFA_BYTES
   uint8_t* sSFB = sSFA + STAGES_P * C::SFA_BYTES;              // STAGES x SFB_BYTES
-  uint8_t* sOut = sSFB + STAGES_P * C::SFB_BYTES;              // OUT_BYTES (1024-aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);
+  uint8_t* sOut = sSFB + STAGES_P * C::SFB_BYTES;              // C::OUT bytes (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT);
   uint64_t* full = bars;                                       // used in rank 0
   uint64_t* empty = bars + STAGES_P;
   uint64_t* acc_full = bars + 2 * STAGES_P;
@@ -752,12 +764,12 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), 8);                         // the epilogue warps of both CTAs
+    mbar_init(smem_u32(acc_empty), 8 * C::EPI_GROUPS);         // the epilogue warps of both CTAs
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < STAGES_P; ++s) mbar_init(smem_u32(&sf_full[s]), 1);
     mbar_init(smem_u32(sf_drain), 1);
     mbar_init(smem_u32(acc_full1), 1);
-    mbar_init(smem_u32(acc_empty1), 8);
+    mbar_init(smem_u32(acc_empty1), 8 * C::EPI_GROUPS);
     *abort_flag = 0;
     *epi_fail = 0;
     fence_mbar_init();
@@ -891,9 +903,10 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       tc_commit_pair_self(smem_u32(sf_drain));                // no copy in flight at exit
       (void)mbar_wait_suspend(smem_u32(sf_drain), 0, p.status);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if ((warp >= 2 && warp <= 5) || warp >= 7) {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;                                    // lane quarter of tensor memory
+    const int grp = warp >= 7 ? 1 : 0;                         // accumulator columns grp * EPI_COLS ..
     const bool leader = (warp == EPI_WARP0 && lane == 0);
     const uint32_t acc_empty_r0 = cluster_map(smem_u32(acc_empty), 0);
     const uint32_t acc_empty1_r0 = cluster_map(smem_u32(acc_empty1), 0);
@@ -905,11 +918,12 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       const int ab = C::NACC == 2 ? (t & 1) : 0;
       const uint32_t aph = C::NACC == 2 ? ((t >> 1) & 1) : (t & 1);
       if (!mbar_wait_suspend(smem_u32(accf(ab)), aph, p.status)) *epi_fail = 1;
-      named_bar(1, 128);
+      named_bar(1, 128 * C::EPI_GROUPS);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<C::BN, C::KIND == KIND_F8, MXOUT>(p, alpha, tmem + ab * C::BN, q, lane, leader, buf, sOut, &map_c, m0,
-                                            tp.n0, [&] {
+      store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT>(
+          p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * (4 * 32 * 33 * 4),
+          &map_c, m0, tp.n0 + grp * C::EPI_COLS, [&] {
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(acce(ab)));
           else mbar_arrive_remote(ab ? acc_empty1_r0 : acc_empty_r0);
@@ -1058,7 +1072,7 @@ int launch(const GemmArgs& g, cudaStream_t st) {
 // kernel); 0 if the device cannot hold one.
 template <int KIND, int MXOUT>
 int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
-              int smem) {
+              int smem, int threads) {
   static int cache[64] = {};
   static bool attr_set[64] = {};
   int dev = 0;
@@ -1070,7 +1084,7 @@ int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, C
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sm_count() / 2));
-  cfg.blockDim = dim3(mxq::gemm::PAIR_THREADS);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1091,7 +1105,7 @@ int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, C
 template <int KIND, int MXOUT>
 int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   using namespace mxq::gemm;
-  using Cf = PairCfg<KIND>;
+  using Cf = PairCfg<KIND, MXOUT>;
   const int64_t kbytes = Cf::FP4 ? g.K / 2 : g.K;
   const int64_t kb4 = g.K / 128;
   CUtensorMap ma, mb, msa, msb, mc;
@@ -1115,7 +1129,7 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   if (!p.status) return MXQ_ERR_CUDA;
   p.tx_bytes = 2 * (tx_bytes(Cf::A_BYTES, g.a_u4) + tx_bytes(Cf::B_BYTES, g.b_u4) + Cf::SFA_BYTES + Cf::SFB_BYTES);
   const int grid = 2 * std::min(p.ntiles, pairs);
-  return launch_pdl_cluster(mx_gemm_pair_kernel<KIND, MXOUT>, dim3(grid), dim3(PAIR_THREADS), Cf::SMEM, st, 2, ma, mb, msa,
+  return launch_pdl_cluster(mx_gemm_pair_kernel<KIND, MXOUT>, dim3(grid), dim3(Cf::THREADS), Cf::SMEM, st, 2, ma, mb, msa,
                             msb, mc, p);
 }
 
@@ -1124,8 +1138,8 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
 template <int KIND, int MXOUT>
 int dispatch_out(const GemmArgs& g, cudaStream_t st) {
   if (g.M % 256 == 0 && g.N % 256 == 0) {
-    const int pairs =
-        max_pairs<KIND, MXOUT>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, mxq::gemm::PairCfg<KIND>::SMEM);
+    using Cf = mxq::gemm::PairCfg<KIND, MXOUT>;
+    const int pairs = max_pairs<KIND, MXOUT>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, Cf::SMEM, Cf::THREADS);
     if (pairs > 0) return launch_pair<KIND, MXOUT>(g, pairs, st);
   }
   return (g.N % 256 == 0) ? launch<KIND, 256, MXOUT>(g, st) : launch<KIND, 128, MXOUT>(g, st);
