@@ -54,10 +54,15 @@ constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int PAIR_THREADS = 224;     // pair kernel: the roles above plus warp 6 (scale copies)
 constexpr int STG_BYTES = BM * 64;       // one staging buffer: 128 rows x 64 B
-// the staging area: two buffers, also the 4 warps' 32 x 33-word transpose
-// scratch of the MX column-block output
-constexpr int OUT_BYTES = 2 * STG_BYTES + 512;
-static_assert(4 * 32 * 33 * 4 <= OUT_BYTES, "transpose scratch");
+// Transpose scratch of one epilogue warp (MX column-block output): its
+// 32 x 32 chunk, row k at word k * XS_PITCH.  A pitch of 36 words keeps
+// 16-byte row writes (eight lanes per access phase, banks 4 k .. 4 k + 3
+// apart) and column reads (lane j at bank 4 k + j) free of bank conflicts.
+constexpr int XS_PITCH = 36;
+constexpr int XS_WORDS = 32 * XS_PITCH;
+constexpr int XS_GROUP_BYTES = 4 * XS_WORDS * 4;    // four epilogue warps
+// the staging area: two buffers, also the four epilogue warps' transpose scratch
+constexpr int OUT_BYTES = std::max(2 * STG_BYTES + 512, XS_GROUP_BYTES);
 
 // Operand kinds (a template parameter of both kernels).
 constexpr int KIND_MXF8 = 0;   // block-scaled E4M3 / E5M2: kind::mxf8f6f4, scale_vec::1X
@@ -272,26 +277,10 @@ __device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt,
   return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
 }
 
-// The same for column `lane` of a warp's 32 x 32 chunk held in shared memory
-// (word k * 33 + j holds row k, column j; the padding keeps both the row
-// writes and the column reads free of bank conflicts): the block's 32 values
-// are read twice (amax, then codes) so that few registers are live.
-__device__ __forceinline__ uint32_t mx_block32_col(const uint32_t* xs, int lane, int fmt, int ceil_mode,
-                                                   uint32_t* codes /* 8 words */) {
-  uint32_t ab = 0;
+// Column `lane` of the warp's chunk, read once from the transpose scratch.
+__device__ __forceinline__ void load_col32(const uint32_t* xs, int lane, uint32_t (&v)[32]) {
 #pragma unroll
-  for (int k = 0; k < 32; ++k) ab = max(ab, xs[k * 33 + lane] & 0x7FFFFFFFu);
-  const bool bad = ab >= 0x7F800000u;
-  const int e = bad ? 0 : (fmt == MXQ_E4M3 ? scale_exp<MXQ_E4M3>(ab, ceil_mode) : scale_exp<MXQ_E5M2>(ab, ceil_mode));
-  const float m = exp2_neg(e);
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    float f[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) f[i] = __fmul_rn(__uint_as_float(xs[(4 * w + i) * 33 + lane]), m);
-    codes[w] = bad ? 0u : fp8x4_rt(fmt, f[0], f[1], f[2], f[3]);
-  }
-  return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+  for (int k = 0; k < 32; ++k) v[k] = xs[k * XS_PITCH + lane];
 }
 
 // Row-block scale words of one output row (BN / 32 scale bytes, four per
@@ -416,7 +405,7 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     // unused) staging area, rows padded to 33 words so that neither the row
     // writes nor the column reads conflict, and lane j quantizes column j.
     uint32_t sc[BN / 128];
-    uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * (32 * 33);   // this warp's 32 x 33 words
+    uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * XS_WORDS;    // this warp's transpose scratch
     const size_t rg = static_cast<size_t>(m0 + row);
     const size_t rT = static_cast<size_t>(m0 + q * 32);          // first row of the warp's column blocks
 #pragma unroll
@@ -439,11 +428,14 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
         }
         if (p.cqT) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[h][j];
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(xs + lane * XS_PITCH + 4 * j) =
+                make_uint4(v[h][4 * j], v[h][4 * j + 1], v[h][4 * j + 2], v[h][4 * j + 3]);
           __syncwarp();
-          uint32_t cc[8];
-          const uint32_t sT = mx_block32_col(xs, lane, p.mx_fmt, p.mx_ceil, cc);
+          uint32_t col[32], cc[8];
+          load_col32(xs, lane, col);
           __syncwarp();
+          const uint32_t sT = mx_block32(col, p.mx_fmt, p.mx_ceil, cc);
           const size_t n = static_cast<size_t>(n0 + (c + h) * 32 + lane);
           uint4* dT = reinterpret_cast<uint4*>(p.cqT + n * static_cast<size_t>(p.M) + rT);
           dT[0] = make_uint4(cc[0], cc[1], cc[2], cc[3]);
@@ -703,7 +695,7 @@ struct PairCfg {
   static constexpr int EPI_COLS = BN / EPI_GROUPS;      // accumulator columns per epilogue group
   static constexpr int THREADS = PAIR_THREADS + (EPI_GROUPS - 1) * 128;
   // the column-block output transposes through 32 x 33 words per epilogue warp
-  static constexpr int OUT = MXOUT_ == 2 ? EPI_GROUPS * 4 * 32 * 33 * 4 : OUT_BYTES;
+  static constexpr int OUT = MXOUT_ == 2 ? EPI_GROUPS * XS_GROUP_BYTES : OUT_BYTES;
   static constexpr int STAGES = (FP4 || MXOUT_ == 2) ? 5 : 6;
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
@@ -922,7 +914,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
       store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT>(
-          p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * (4 * 32 * 33 * 4),
+          p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * XS_GROUP_BYTES,
           &map_c, m0, tp.n0 + grp * C::EPI_COLS, [&] {
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(acce(ab)));
