@@ -458,6 +458,33 @@ def test_gemm_mixed_formats_decode_each_operand():
     assert np.array_equal(sub, ref[:5, :7])
 
 
+def test_gemm_fp8_x_fp4_unpacks_the_packed_operand():
+    """A in E4M3 times B in packed E2M1 (two codes per byte, low nibble the
+    even column) with unit rows: C[:, n] is A's dequantized column cols[n]
+    times B's value, each value a top-binade E2M1 element after its block
+    scale.  The non-zeros sit at odd and even columns, so a swapped nibble
+    order moves them to the neighbouring column; decoding B with A's format
+    fails too.  The operands swapped give the transpose."""
+    rng = np.random.default_rng(17)
+    M, N, K = 64, 32, 128
+    a = rng.standard_normal((M, K))
+    A = mx.quantize(a, F.E4M3, mx.ROW)
+    cols = rng.choice(K, N, replace=False)
+    assert len(set(cols % 2)) == 2
+    vals = rng.choice([1.0, 1.5, 3.0, -6.0], N) * np.exp2(rng.integers(-6, 7, N))
+    b = np.zeros((N, K))
+    b[np.arange(N), cols] = vals
+    B = mx.quantize(b, F.E2M1, mx.ROW)
+    assert B["q_row"].shape == (N, K // 2)
+    deqA = mx.dequantize(A["q_row"], A["s_row"], F.E4M3)
+    ref = gemm.reference(A["q_row"], A["s_row"], B["q_row"], B["s_row"], F.E4M3, F.E2M1)
+    assert np.array_equal(ref, deqA[:, cols] * vals)
+    ref_t = gemm.reference(B["q_row"], B["s_row"], A["q_row"], A["s_row"], F.E2M1, F.E4M3)
+    assert np.array_equal(ref_t, ref.T)
+    swapped = ((B["q_row"] >> 4) | (B["q_row"] << 4)).astype(np.uint8)
+    assert not np.array_equal(gemm.reference(A["q_row"], A["s_row"], swapped, B["s_row"], F.E4M3, F.E2M1), ref)
+
+
 def test_mm_fp8_reference_one_hot_rows_index_b():
     """One-hot A rows (code for 1.0 at column perm[m]) pick B's columns:
     C[m, n] = dec(b)[n, perm[m]] * scale + bias[n], read off by indexing
