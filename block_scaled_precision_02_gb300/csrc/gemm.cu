@@ -36,7 +36,13 @@
 //  * warps 2..5  epilogue: tcgen05.ld of this CTA's 128 x N float32
 //                accumulator rows (each thread owns one row), conversion,
 //                and stores (TMA through two 64-byte-swizzled staging
-//                buffers; the MX output is stored directly).
+//                buffers; the MX output is stored directly).  The pair
+//                kernel's MX-output variants add warps 7..10, a second
+//                epilogue group that takes the other half of the columns.
+// Operands: E4M3 / E5M2 / E2M1 in any pairing.  Packed E2M1 beside an 8-bit
+// operand is widened to one byte per code by its tensor map on the way into
+// shared memory (the 4-bit layout of kind::mxf8f6f4), so both operands then
+// share the 8-bit tile layout.
 // Every wait is bounded (1 s); on expiry the status word records
 // MXQ_ERR_TIMEOUT, all roles wind down, in-flight copies are awaited (with a
 // limit) and tensor memory is released.
