@@ -97,6 +97,54 @@ def _cuda_2d(x: torch.Tensor, name: str):
         raise ValueError(f"{name} must be a 2-D CUDA tensor")
 
 
+# Argument checks that keep a wrong call from reaching a kernel: every device
+# pointer the library dereferences must be a CUDA tensor on the call's device
+# holding at least the bytes the call reads.  Structural checks come first.
+def _on_device(ts, device: torch.device):
+    for t, name in ts:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
+
+
+def _byte_tensor(t: torch.Tensor, name: str, numel: Optional[int] = None):
+    """Codes or scales: contiguous, one byte per element (uint8 or a float8
+    dtype), and exactly ``numel`` elements when given."""
+    if not isinstance(t, torch.Tensor) or t.element_size() != 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of 1-byte elements")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} holds {t.numel()} bytes, expected {numel}")
+
+
+def _mx_operands(a_q, a_s, f, b_q, b_s, fb, K):
+    """(M, N, K) of a block-scaled product, after checking that A [M][K] and
+    B [N][K] agree on K (E2M1 codes packed two per byte) and that each scale
+    tensor holds one byte per row per 32 elements of K."""
+    for t, name in ((a_q, "a_q"), (b_q, "b_q")):
+        if not isinstance(t, torch.Tensor) or t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D tensor of codes")
+    M, N = a_q.shape[0], b_q.shape[0]
+    ka = a_q.shape[1] * (2 if f == E2M1 else 1)
+    kb = b_q.shape[1] * (2 if fb == E2M1 else 1)
+    if K is None:
+        K = ka
+    if ka != K or kb != K:
+        raise ValueError(f"K differs: a_q holds {ka}, b_q {kb}, K = {K}")
+    _byte_tensor(a_q, "a_q")
+    _byte_tensor(b_q, "b_q")
+    if K % 32 == 0:
+        _byte_tensor(a_s, "a_s", M * (K // 32))
+        _byte_tensor(b_s, "b_s", N * (K // 32))
+    else:
+        _byte_tensor(a_s, "a_s")
+        _byte_tensor(b_s, "b_s")
+    _on_device(((a_q, "a_q"), (a_s, "a_s"), (b_q, "b_q"), (b_s, "b_s")), a_q.device)
+    return M, N, K
+
+
 # --------------------------------------------------------------------------- MX quantize
 def mx_quantize(x: torch.Tensor, fmt="e4m3", orientation="row", scale_mode="floor", rounding="rne",
                 hadamard32: bool = False, sr_key: int = 0, hadamard_seed: int = 7, sf_layout="canonical"):
@@ -127,10 +175,16 @@ def mx_quantize(x: torch.Tensor, fmt="e4m3", orientation="row", scale_mode="floo
 
 def mx_dequantize(q: torch.Tensor, s: torch.Tensor, fmt="e4m3", out_dtype=torch.float32) -> torch.Tensor:
     """Dequantize codes ``q`` with canonical scales ``s`` -> float32 or bf16."""
-    _cuda_2d(q, "q")
     f = _FMT[fmt]
+    if not isinstance(q, torch.Tensor) or q.dim() != 2:
+        raise ValueError("q must be a 2-D tensor of codes")
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     rows = q.shape[0]
     cols = q.shape[1] * (2 if f == E2M1 else 1)
+    _byte_tensor(q, "q")
+    _byte_tensor(s, "s", rows * (cols // 32) if cols % 32 == 0 else None)
+    _on_device(((q, "q"), (s, "s")), q.device)
     out = torch.empty(rows, cols, dtype=out_dtype, device=q.device)
     rc = load().mxq_dequantize(_ptr(q), _ptr(s), rows, cols, f, int(out_dtype == torch.float32), _ptr(out),
                                _stream(q.device))
@@ -152,6 +206,12 @@ def fp8_quantize_pertensor(x: torch.Tensor, scale: torch.Tensor, fmt="e4m3", ori
     f, o = _FMT[fmt], _ORIENT[orientation]
     if f not in (E4M3, E5M2):
         raise ValueError(f"unsupported fp8 format {fmt!r} (expected 'e4m3' or 'e5m2')")
+    if not isinstance(scale, torch.Tensor) or scale.dtype != torch.float32 or scale.numel() < 1:
+        raise ValueError("scale must be a float32 device tensor (its first element is the multiplier)")
+    if ring_state is not None and (ring_state.dtype != torch.float32 or not ring_state.is_contiguous()
+                                   or ring_state.numel() < 5):
+        raise ValueError("ring_state must be a contiguous float32 tensor of hist_len + 4 >= 5 elements")
+    _on_device(((scale, "scale"), (ring_state, "ring_state")), x.device)
     rows, cols = x.shape
     dev = x.device
     x8 = torch.empty(rows, cols, dtype=torch.uint8, device=dev) if o & ROW else None
@@ -201,10 +261,9 @@ def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.
     one runs at the 8-bit rate).  Returns bf16 (or float32) [M][N]."""
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
-    M = a_q.shape[0]
-    N = b_q.shape[0]
-    if K is None:
-        K = a_q.shape[1] * (2 if f == E2M1 else 1)
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    M, N, K = _mx_operands(a_q, a_s, f, b_q, b_s, fb, K)
     c = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
     if fb == f:
         rc = load().mxq_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout], _ptr(c),
@@ -228,10 +287,7 @@ def mx_gemm_mx_out(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s:
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
     o = _ORIENT[orientation]
-    M = a_q.shape[0]
-    N = b_q.shape[0]
-    if K is None:
-        K = a_q.shape[1] * (2 if f == E2M1 else 1)
+    M, N, K = _mx_operands(a_q, a_s, f, b_q, b_s, fb, K)
     dev = a_q.device
     cq = cs = cqT = csT = None
     if o & ROW:
@@ -282,10 +338,13 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
         raise ValueError("a's batch entries must be contiguous")
     if B.dim() == 3 and bb > 1 and B.stride(0) != N * K:
         raise ValueError("b's batch entries must be contiguous")
+    if a.element_size() != 1 or b.element_size() != 1:
+        raise ValueError("a and b must hold 1-byte FP8 codes (uint8 or a torch float8 dtype)")
     if scale.dtype != torch.float32 or scale.numel() != 1 or not scale.is_cuda:
         raise ValueError("scale must be a 1-element float32 CUDA tensor")
     if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
         raise ValueError("bias must be a contiguous bf16 vector of length n")
+    _on_device(((a, "a"), (b, "b"), (scale, "scale"), (bias, "bias")), a.device)
     shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
     c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
     rc = load().mxq_mm_fp8(_ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), f, _ptr(scale),
@@ -296,6 +355,10 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
 
 def sf_to_mma(s: torch.Tensor) -> torch.Tensor:
     """Canonical scales [rows][kb] -> the GEMM's 512-byte-chunk layout (flat)."""
+    if not isinstance(s, torch.Tensor) or s.dim() != 2:
+        raise ValueError("s must be a 2-D tensor of scales [rows][kb]")
+    _byte_tensor(s, "s")
+    _on_device(((s, "s"),), s.device)
     out = torch.empty(s.numel(), dtype=torch.uint8, device=s.device)
     rc = load().mxq_sf_to_mma(_ptr(s), s.shape[0], s.shape[1], _ptr(out), _stream(s.device))
     _check(rc, "mxq_sf_to_mma")

@@ -1,0 +1,67 @@
+"""The Python binding refuses, before any library call, arguments that would
+send a kernel a host pointer or fewer bytes than it reads: operands that
+disagree on K, scale tensors of the wrong size, wide element types, and
+tensors that are not on the GPU.  CPU only: every call here raises."""
+
+import pytest
+import torch
+
+import block_scaled_precision_02_gb300 as mxq
+
+
+def u8(*shape):
+    return torch.zeros(*shape, dtype=torch.uint8)
+
+
+def test_gemm_operands_must_agree_on_k():
+    with pytest.raises(ValueError, match="K differs"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 256), u8(256 * 8), "e4m3")
+    # packed E2M1 beside E4M3: 256 bytes of E2M1 codes are 512 elements
+    with pytest.raises(ValueError, match="K differs"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 512), u8(256 * 32), "e4m3", b_fmt="e2m1")
+    with pytest.raises(ValueError, match="K differs"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 512), u8(256 * 16), "e4m3", K=1024)
+    with pytest.raises(ValueError, match="K differs"):
+        mxq.mx_gemm_mx_out(u8(256, 512), u8(256 * 16), u8(256, 256), u8(256 * 8), "e4m3")
+
+
+def test_gemm_scales_must_cover_every_block():
+    with pytest.raises(ValueError, match="a_s holds"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 15), u8(256, 512), u8(256 * 16), "e4m3")
+    with pytest.raises(ValueError, match="b_s holds"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(128, 512), u8(256 * 16), "e4m3")
+    with pytest.raises(ValueError, match="b_s holds"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 256), u8(256 * 8), "e4m3", b_fmt="e2m1")
+
+
+def test_gemm_operands_must_be_byte_codes_on_the_gpu():
+    with pytest.raises(ValueError, match="1-byte elements"):
+        mxq.mx_gemm(torch.zeros(256, 512, dtype=torch.bfloat16), u8(256 * 16), u8(256, 512), u8(256 * 16))
+    with pytest.raises(ValueError, match="1-byte elements"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 512).t().contiguous().t(), u8(256 * 16))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 512), u8(256 * 16), "e4m3")
+    with pytest.raises(ValueError, match="out_dtype"):
+        mxq.mx_gemm(u8(256, 512), u8(256 * 16), u8(256, 512), u8(256 * 16), out_dtype=torch.float16)
+
+
+def test_dequantize_checks_scales_and_device():
+    with pytest.raises(ValueError, match="s holds"):
+        mxq.mx_dequantize(u8(64, 64), u8(64, 1), "e4m3")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mxq.mx_dequantize(u8(64, 64), u8(64, 2), "e4m3")
+    with pytest.raises(ValueError, match="out_dtype"):
+        mxq.mx_dequantize(u8(64, 64), u8(64, 2), "e4m3", torch.int32)
+
+
+def test_mm_fp8_needs_byte_codes():
+    a = torch.zeros(128, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="1-byte FP8 codes"):
+        mxq.mm_fp8(a, a.t(), torch.ones(1))
+
+
+def test_sf_to_mma_needs_a_gpu_tensor():
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mxq.sf_to_mma(u8(128, 4))
+    with pytest.raises(ValueError, match="2-D"):
+        mxq.sf_to_mma(u8(512))
