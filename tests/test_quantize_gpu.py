@@ -151,6 +151,19 @@ def test_stochastic_rounding_four_draws_per_call(lib, fmt, orient):
             check(got, ref, orient)
 
 
+@pytest.mark.parametrize("fmt", ["e2m1", "e4m3", "e5m2"])
+@pytest.mark.parametrize("orient", ["row", "col", "dual"])
+@pytest.mark.parametrize("rounding", ["sr", "sr4"])
+def test_stochastic_rounding_ceil_scales(lib, fmt, orient, rounding):
+    """Stochastic rounding under the ceil scale rule, with and without the
+    Hadamard: the scale never saturates a block, so every element rounds
+    between two in-range neighbours."""
+    g = inputs.heavy_gradient(160, 288, seed=12)
+    for had in (False, True):
+        got, ref = run_both(lib, g, fmt, orient, "ceil", rounding, had, 0x5EED, 7)
+        check(got, ref, orient)
+
+
 def test_sr4_differs_from_sr_and_is_deterministic(lib):
     g = inputs.heavy_gradient(128, 256, seed=2).cuda()
     a = lib.mx_quantize(g, "e2m1", "row", "floor", "sr4", True, 3, 7)
@@ -300,6 +313,20 @@ def test_full_size_fp4_sr_hadamard_sampled(lib):
     gv = f64(g)
     rows = _sample_rows(4096, 24, 3)
     ref = omx.quantize(gv[rows], F.E2M1, omx.ROW, omx.FLOOR, omx.SR, True, 0, 7, row_index=rows, total_cols=14336)
+    assert_bytes_equal(np_(q)[rows], ref["q_row"], "q sample")
+    s_can = omx.sf_from_mma(np_(s), 4096, 14336 // 32)
+    assert_bytes_equal(s_can[rows], ref["s_row"], "s sample")
+
+
+def test_full_size_fp4_sr_hadamard_ceil_sampled(lib):
+    """The same 4096 x 14336 MXFP4 quantize under ceil scales (both scale
+    rules of the recipe are timed), sampled rows."""
+    g = inputs.heavy_gradient()
+    dev = torch.device("cuda")
+    q, s, _, _ = lib.mx_quantize(g.to(dev), "e2m1", "row", "ceil", "sr", True, 0, 7, "mma")
+    gv = f64(g)
+    rows = _sample_rows(4096, 24, 5)
+    ref = omx.quantize(gv[rows], F.E2M1, omx.ROW, omx.CEIL, omx.SR, True, 0, 7, row_index=rows, total_cols=14336)
     assert_bytes_equal(np_(q)[rows], ref["q_row"], "q sample")
     s_can = omx.sf_from_mma(np_(s), 4096, 14336 // 32)
     assert_bytes_equal(s_can[rows], ref["s_row"], "s sample")
