@@ -116,6 +116,34 @@ def test_mx_output_exact_fp8_x_fp4(lib, fa, fb, mnk):
     assert_bytes_equal(csT, want["s_col"], "column-block scales")
 
 
+@pytest.mark.parametrize("orientation", ["row", "col", "dual"])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 512)])
+def test_mx_output_exact_mxfp4_operands(lib, orientation, layout, mnk):
+    """The MX output of an MXFP4 x MXFP4 product (kind::mxf4): A = +-2^j per
+    row and B = integers in [-4, 4] are exact in E2M1, every sum is exact in
+    float32, so the output blocks equal the oracle's quantization of the
+    float64 product bit for bit, on the single-CTA kernel (M = 128) and the
+    CTA pair."""
+    M, N, K = mnk
+    rng = np.random.default_rng(29)
+    a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
+    b = rng.integers(-4, 5, (N, K)).astype(np.float64)
+    ra = omx.quantize(a, F.E2M1, omx.ROW, omx.FLOOR)
+    rb = omx.quantize(b, F.E2M1, omx.ROW, omx.FLOOR)
+    aq, as_, bq, bs = ra["q_row"], ra["s_row"], rb["q_row"], rb["s_row"]
+    ref = og.reference(aq, as_, bq, bs, F.E2M1)
+    assert np.array_equal(ref, a @ b.T)                          # the operands quantize exactly
+    want = omx.quantize(ref, F.E4M3, omx.DUAL, omx.FLOOR)
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e2m1", "e4m3", "floor", layout, orientation)
+    if orientation in ("row", "dual"):
+        assert_bytes_equal(cq, want["q_row"], "codes")
+        assert_bytes_equal(cs, want["s_row"], "scales")
+    if orientation in ("col", "dual"):
+        assert_bytes_equal(cqT, want["q_col"], "column-block codes")
+        assert_bytes_equal(csT, want["s_col"], "column-block scales")
+
+
 def e4m3_spacing(y):
     """Grid spacing of E4M3 at magnitude y (3 mantissa bits; subnormal step 2^-9)."""
     a = np.abs(y)
