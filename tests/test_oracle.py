@@ -267,6 +267,60 @@ def test_fwht_matches_dense_sylvester_exactly():
     assert np.array_equal(back, v.astype(np.float64))
 
 
+def _fwht_tie_blocks():
+    """Two blocks whose butterflies produce a float32 tie: 1 and 2^-24 meet
+    at the first stage (positions 0 and 1) or at the last (0 and 16)."""
+    v = np.zeros((2, 32), dtype=np.float32)
+    v[:, 0] = 1.0
+    v[0, 1] = 2.0 ** -24
+    v[1, 16] = 2.0 ** -24
+    return v
+
+
+def _fwht_tie_expected(seed=7):
+    """Expected outputs of _fwht_tie_blocks, worked by hand.
+
+    Block 0: the h = 1 butterfly gives u0 = s0 + s1 e and u1 = s0 - s1 e
+    (e = 2^-24).  One of them has magnitude 1 + e, the midpoint of 1 and the
+    next float32 1 + 2^-23, so it rounds to magnitude 1 (even mantissa); the
+    other, 1 - e, is a float32.  Every later butterfly pairs a value with a
+    zero, (u, 0) -> (u, u), which is exact, so y_j = RN32(w_(j mod 2) * c).
+    Block 1: stages h = 1..8 copy s0 over positions 0..15 and s16 e over
+    16..31 (exact); stage 16 gives s0 + s16 e on 0..15 and s0 - s16 e on
+    16..31, rounded as above, so y_j = RN32(w_(j >= 16) * c).
+    With c in [1/8, 1/4) (float32 step 2^-26) and c e = 0.707.. * 2^-26:
+    RN32(1 * c) = c and RN32((1 - e) c) = c - 2^-26.  (A float64 transform
+    rounded once would give RN32((1 + e) c) = c + 2^-26 instead of c.)
+    The signs s_j are the pinned seed-7 signs."""
+    s = philox.hadamard_signs(seed)
+    c = float(mx.HADAMARD_C)
+    step = 2.0 ** -26
+    assert 0.125 <= c < 0.25
+
+    def pair(sa, sb):
+        # (value on the "+" side, value on the "-" side) after RN32 of each
+        # butterfly output times c
+        plus, minus = (c, c - step) if sa == sb else (c - step, c)
+        return sa * plus, sa * minus
+
+    out = np.zeros((2, 32))
+    p0, m0 = pair(s[0], s[1])
+    out[0, 0::2], out[0, 1::2] = p0, m0
+    p1, m1 = pair(s[0], s[16])
+    out[1, :16], out[1, 16:] = p1, m1
+    return out
+
+
+def test_fwht_rounds_every_butterfly_to_float32():
+    """The Hadamard rounds each butterfly output to float32 (ties to even),
+    at the first stage and at the last, then RN32(u * c): the hand-worked
+    values of _fwht_tie_expected."""
+    got = mx.hadamard32_blocks(_fwht_tie_blocks(), 7).astype(np.float64)
+    want = _fwht_tie_expected(7)
+    assert np.array_equal(got, want)
+    assert np.all(np.abs(got) > 0)
+
+
 def test_hadamard_constant_is_nearest_float32():
     c = Fraction(float(mx.HADAMARD_C))
     ulp = Fraction(2) ** (math.frexp(float(mx.HADAMARD_C))[1] - 24)
@@ -388,6 +442,43 @@ def test_pertensor_transposed_byte_equality_and_amax():
         # multiplier 1 and values on the grid are kept exactly
         g = F.decode(f, np.arange(0, 0x70)).astype(np.float64)
         assert np.array_equal(F.decode(f, pertensor.quantize_pertensor(g[None, :], 1.0, f)[0])[0], g)
+
+
+def _pt_cases():
+    """(x, m, fmt, code under RN32 of the product, code of the exact product)
+    -- the hand-worked cases of test_pertensor_product_is_rounded_to_float32."""
+    x = 1.0 + 2.0 ** -7                          # a bf16 value: 129 * 2^-7
+    return [
+        (x, 8843804 * 2.0 ** -23, F.E4M3, 0x38, 0x39),
+        (x, 9884251 * 2.0 ** -23, F.E4M3, 0x3A, 0x39),
+        (x, 9364028 * 2.0 ** -23, F.E5M2, 0x3C, 0x3D),
+        (-x, 8843804 * 2.0 ** -23, F.E4M3, 0xB8, 0xB9),
+    ]
+
+
+def test_pertensor_product_is_rounded_to_float32():
+    """x8 = encode(RN32(x * m)): the product is rounded to float32 once, and
+    that rounding can land on an element-grid midpoint, where the tie goes to
+    the even code.  Hand-worked (x = 129 * 2^-7, m = k * 2^-23, so
+    x * m = 129 k * 2^-30 exactly; a float32 step in [1, 2) is 128 * 2^-30):
+
+    * E4M3, k = 8843804: x * m = 1140850716 * 2^-30 = 1.0625 + 28 * 2^-30.
+      28 < 64, so RN32 gives 1.0625, the midpoint of 1.0 (0x38, mantissa 000)
+      and 1.125 (0x39, mantissa 001): even code 0x38.  The exact product lies
+      above the midpoint and would encode to 0x39.
+    * E4M3, k = 9884251: x * m = 1275068379 * 2^-30 = 1.1875 - 37 * 2^-30.
+      RN32 gives 1.1875, the midpoint of 1.125 (0x39) and 1.25 (0x3A,
+      mantissa 010): 0x3A.  The exact product lies below it: 0x39.
+    * E5M2, k = 9364028: x * m = 1207959612 * 2^-30 = 1.125 + 60 * 2^-30.
+      RN32 gives 1.125, the midpoint of 1.0 (0x3C) and 1.25 (0x3D): 0x3C.
+      The exact product: 0x3D.
+    * the first case negated: the sign bit is set, 0xB8 (exact product 0xB9).
+    """
+    for x, m, f, want, _ in _pt_cases():
+        assert np.float32(m) == m                 # m is a float32 multiplier
+        x8, x8T, amax = pertensor.quantize_pertensor(np.array([[x]]), m, f)
+        assert int(x8[0, 0]) == want and int(x8T[0, 0]) == want
+        assert amax == abs(x)
 
 
 def test_ring_fold_sixteen_steps_closed_form():
@@ -562,6 +653,29 @@ def test_planted_fwht_sign_error_is_caught(monkeypatch):
     want = (dense.astype(np.float32) * mx.HADAMARD_C)
     assert np.array_equal(orig(v, 7), want)
     assert not np.array_equal(wrong(v, 7), want)
+
+
+def test_planted_fwht_rounded_once_is_caught():
+    """A transform done exactly in float64 and rounded to float32 only at the
+    end must fail the per-butterfly rounding pin."""
+    def rounded_once(v32, seed):
+        u = np.asarray(v32, dtype=np.float64) * philox.hadamard_signs(seed)
+        y = u @ mx.sylvester(32).T.astype(np.float64)             # exact sums
+        return (y * np.float64(mx.HADAMARD_C)).astype(np.float32)
+
+    v = _fwht_tie_blocks()
+    want = _fwht_tie_expected(7)
+    assert np.array_equal(mx.hadamard32_blocks(v, 7).astype(np.float64), want)
+    assert not np.array_equal(rounded_once(v, 7).astype(np.float64), want)
+
+
+def test_planted_pertensor_exact_product_is_caught():
+    """Encoding the exact float64 product x * m (no float32 rounding first)
+    must fail the per-tensor pin."""
+    for x, m, f, want, exact_code in _pt_cases():
+        wrong = F.encode_rne_sat(f, np.array([[x]]) * np.float64(np.float32(m)))
+        assert int(wrong[0, 0]) == exact_code != want
+        assert int(pertensor.quantize_pertensor(np.array([[x]]), m, f)[0][0, 0]) == want
 
 
 def test_planted_sr_direction_error_is_caught():
