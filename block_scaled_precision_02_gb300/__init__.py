@@ -92,6 +92,18 @@ def _check(rc: int, what: str):
         raise MXQError(rc, what)
 
 
+def _call(name: str, device: torch.device, *args) -> None:
+    """Run library entry point ``name`` with ``device`` current and torch's
+    current stream of that device appended as the last argument; raise on a
+    non-zero status.  The library launches on the current device and keys
+    its per-device state (status word, SM count, occupancy) on it, and the
+    stream handle must belong to that device, so every call makes the
+    tensors' device current first (restoring the previous one after)."""
+    with torch.cuda.device(device):
+        rc = getattr(load(), name)(*args, _stream(device))
+    _check(rc, name)
+
+
 def _cuda_2d(x: torch.Tensor, name: str):
     if not x.is_cuda or x.dim() != 2:
         raise ValueError(f"{name} must be a 2-D CUDA tensor")
@@ -107,7 +119,7 @@ def _on_device(ts, device: torch.device):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
         if t.device != device:
-            raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
+            raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
 
 
 def _byte_tensor(t: torch.Tensor, name: str, numel: Optional[int] = None):
@@ -166,10 +178,9 @@ def mx_quantize(x: torch.Tensor, fmt="e4m3", orientation="row", scale_mode="floo
     if o & COL:
         q_col = torch.empty(cols, rows // qb, dtype=torch.uint8, device=dev)
         s_col = torch.empty(cols, rows // 32, dtype=torch.uint8, device=dev)
-    rc = load().mxq_quantize(_ptr(x), rows, cols, x.stride(0), f, o, _SCALE[scale_mode], _ROUND[rounding],
-                             int(bool(hadamard32)), sr_key & (2**64 - 1), hadamard_seed & (2**64 - 1),
-                             _SF[sf_layout], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(dev))
-    _check(rc, "mxq_quantize")
+    _call("mxq_quantize", dev, _ptr(x), rows, cols, x.stride(0), f, o, _SCALE[scale_mode], _ROUND[rounding],
+          int(bool(hadamard32)), sr_key & (2**64 - 1), hadamard_seed & (2**64 - 1), _SF[sf_layout], _ptr(q_row),
+          _ptr(s_row), _ptr(q_col), _ptr(s_col))
     return q_row, s_row, q_col, s_col
 
 
@@ -186,9 +197,7 @@ def mx_dequantize(q: torch.Tensor, s: torch.Tensor, fmt="e4m3", out_dtype=torch.
     _byte_tensor(s, "s", rows * (cols // 32) if cols % 32 == 0 else None)
     _on_device(((q, "q"), (s, "s")), q.device)
     out = torch.empty(rows, cols, dtype=out_dtype, device=q.device)
-    rc = load().mxq_dequantize(_ptr(q), _ptr(s), rows, cols, f, int(out_dtype == torch.float32), _ptr(out),
-                               _stream(q.device))
-    _check(rc, "mxq_dequantize")
+    _call("mxq_dequantize", q.device, _ptr(q), _ptr(s), rows, cols, f, int(out_dtype == torch.float32), _ptr(out))
     return out
 
 
@@ -224,10 +233,8 @@ def fp8_quantize_pertensor(x: torch.Tensor, scale: torch.Tensor, fmt="e4m3", ori
     else:
         amax = torch.empty(1, dtype=torch.float32, device=dev)
         amax_out = amax
-    rc = load().fp8_quantize_pertensor(_ptr(x), rows, cols, _ptr(scale), f, o, _ptr(ring_state), n, hist_idx,
-                                       float(fp8_max), float(pow2_margin), _ptr(x8), _ptr(x8T), _ptr(amax_out),
-                                       _stream(dev))
-    _check(rc, "fp8_quantize_pertensor")
+    _call("fp8_quantize_pertensor", dev, _ptr(x), rows, cols, _ptr(scale), f, o, _ptr(ring_state), n, hist_idx,
+          float(fp8_max), float(pow2_margin), _ptr(x8), _ptr(x8T), _ptr(amax_out))
     return x8, x8T, amax
 
 
@@ -266,12 +273,11 @@ def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.
     M, N, K = _mx_operands(a_q, a_s, f, b_q, b_s, fb, K)
     c = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
     if fb == f:
-        rc = load().mxq_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout], _ptr(c),
-                             int(out_dtype == torch.float32), _stream(a_q.device))
+        _call("mxq_gemm", a_q.device, _ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout],
+              _ptr(c), int(out_dtype == torch.float32))
     else:
-        rc = load().mxq_gemm_mixed(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, _SF[sf_layout],
-                                   _ptr(c), int(out_dtype == torch.float32), _stream(a_q.device))
-    _check(rc, "mxq_gemm")
+        _call("mxq_gemm_mixed", a_q.device, _ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K,
+              _SF[sf_layout], _ptr(c), int(out_dtype == torch.float32))
     return c
 
 
@@ -296,10 +302,8 @@ def mx_gemm_mx_out(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s:
     if o & COL:
         cqT = torch.empty(N, M, dtype=torch.uint8, device=dev)
         csT = torch.empty(N, M // 32, dtype=torch.uint8, device=dev)
-    rc = load().mxq_gemm_mx_out(_ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, SF_MMA, _FMT[out_fmt],
-                                _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _ptr(cqT),
-                                _ptr(csT), _stream(dev))
-    _check(rc, "mxq_gemm_mx_out")
+    _call("mxq_gemm_mx_out", dev, _ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, SF_MMA,
+          _FMT[out_fmt], _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _ptr(cqT), _ptr(csT))
     return cq, cs, cqT, csT
 
 
@@ -347,9 +351,8 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
     _on_device(((a, "a"), (b, "b"), (scale, "scale"), (bias, "bias")), a.device)
     shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
     c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
-    rc = load().mxq_mm_fp8(_ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), f, _ptr(scale),
-                           _ptr(bias), _ptr(c), _stream(a.device))
-    _check(rc, "mxq_mm_fp8")
+    _call("mxq_mm_fp8", a.device, _ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), f, _ptr(scale),
+          _ptr(bias), _ptr(c))
     return c
 
 
@@ -360,11 +363,13 @@ def sf_to_mma(s: torch.Tensor) -> torch.Tensor:
     _byte_tensor(s, "s")
     _on_device(((s, "s"),), s.device)
     out = torch.empty(s.numel(), dtype=torch.uint8, device=s.device)
-    rc = load().mxq_sf_to_mma(_ptr(s), s.shape[0], s.shape[1], _ptr(out), _stream(s.device))
-    _check(rc, "mxq_sf_to_mma")
+    _call("mxq_sf_to_mma", s.device, _ptr(s), s.shape[0], s.shape[1], _ptr(out))
     return out
 
 
 def last_device_status(device=None) -> int:
-    dev = torch.device("cuda") if device is None else torch.device(device)
-    return load().mxq_last_device_status(_stream(dev))
+    """Synchronize the device's current stream and return (then clear) the
+    library's device status word of that device (0, or MXQ_ERR_TIMEOUT)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return load().mxq_last_device_status(_stream(dev))

@@ -65,3 +65,44 @@ def test_sf_to_mma_needs_a_gpu_tensor():
         mxq.sf_to_mma(u8(128, 4))
     with pytest.raises(ValueError, match="2-D"):
         mxq.sf_to_mma(u8(512))
+
+
+def test_every_library_call_runs_with_the_tensors_device_current(monkeypatch):
+    """The library launches on the current device and takes the stream of
+    that device: each entry point of the binding calls the library through
+    _call, which makes the tensors' device current around the call."""
+    import ast
+    import inspect
+    src = inspect.getsource(mxq)
+    tree = ast.parse(src)
+    direct = []
+    for fn in ast.walk(tree):
+        if isinstance(fn, ast.FunctionDef) and fn.name not in ("_call", "load", "lib", "last_device_status"):
+            for node in ast.walk(fn):
+                if (isinstance(node, ast.Call) and isinstance(node.func, ast.Attribute)
+                        and isinstance(node.func.value, ast.Call) and getattr(node.func.value.func, "id", "") == "load"):
+                    direct.append(fn.name)
+    assert direct == [], f"library called without the device guard in {direct}"
+
+    events = []
+
+    class FakeDevice:
+        def __init__(self, d):
+            self.d = d
+
+        def __enter__(self):
+            events.append(("enter", str(self.d)))
+
+        def __exit__(self, *a):
+            events.append(("exit", str(self.d)))
+
+    class FakeLib:
+        def mxq_sf_to_mma(self, *args):
+            events.append(("call", args[-1]))
+            return 0
+
+    monkeypatch.setattr(mxq.torch.cuda, "device", FakeDevice)
+    monkeypatch.setattr(mxq, "_stream", lambda d: f"stream of {d}")
+    monkeypatch.setattr(mxq, "load", lambda: FakeLib())
+    mxq._call("mxq_sf_to_mma", torch.device("cuda", 1), 1, 2)
+    assert events == [("enter", "cuda:1"), ("call", "stream of cuda:1"), ("exit", "cuda:1")]
