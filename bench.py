@@ -348,13 +348,18 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
 
 def pertensor_part(args, mxq, X, timed):
     """Per-tensor FP8 E4M3 dual quantize of 4096 x 14336 with the in-kernel
-    fold into a 16-entry history, steps taken in sequence."""
+    fold into a 16-entry history, steps taken in sequence: step t quantizes
+    base * 2^v_t (v_t from the seeded step law, the 16 step inputs resident
+    on the device) with the multiplier the previous fold published."""
+    from block_scaled_precision_02_gb300 import inputs
     X3 = X["X3"]
+    xs = [inputs.pertensor_step(X3, v) for v in inputs.pertensor_step_exponents(16, seed=3)]
     ring = mxq.ring_state_new(16, X3.device)
     t3 = {"k": 0}
 
     def pt():
-        mxq.quantize_dual(X3, ring[17:18], "e4m3", ring, t3["k"] % 16)
+        t = t3["k"] % 16
+        mxq.quantize_dual(xs[t], ring[17:18], "e4m3", ring, t)
         t3["k"] += 1
     for _ in range(3):
         pt()
@@ -362,7 +367,8 @@ def pertensor_part(args, mxq, X, timed):
     ms_dual = timed(pt, k)
 
     def ptt():                              # transposed output only (x8T), same ring
-        mxq.quantize(X3, ring[17:18], "e4m3", True, ring, t3["k"] % 16)
+        t = t3["k"] % 16
+        mxq.quantize(xs[t], ring[17:18], "e4m3", True, ring, t)
         t3["k"] += 1
     for _ in range(3):
         ptt()

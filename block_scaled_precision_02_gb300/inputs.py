@@ -83,6 +83,13 @@ def pertensor_step_exponents(steps: int = 16, seed: int = 3) -> list[int]:
     return [int(v) for v in rng.integers(-4, 5, size=steps)]
 
 
+def pertensor_step(base: torch.Tensor, v: int) -> torch.Tensor:
+    """Step input x_t = base * 2^v (bf16, on base's device).  A power-of-two
+    factor is exact in bf16 for these magnitudes, so every step's values are
+    the base's, shifted in exponent."""
+    return (base.float() * (2.0 ** v)).to(torch.bfloat16)
+
+
 def weights(rows: int = 4096, cols: int = 4096, seed: int = 4) -> torch.Tensor:
     return normal(rows, cols, 0.02, seed)
 

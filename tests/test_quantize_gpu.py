@@ -89,24 +89,49 @@ def test_dequant_other_formats(lib, fmt):
     assert_bytes_equal(np_(d).view(np.uint32), want.view(np.uint32), "dequant")
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
-def test_special_values_and_edge_blocks(lib, fmt):
-    """Zero blocks (both signs), subnormal bf16, saturation, exact ties, NaN
-    and Inf blocks (scale 0xFF, zero codes)."""
+def _edge_blocks():
+    """128 x 128 bf16 of awkward values: zero blocks of both signs, bf16
+    subnormals, values above every format maximum (3e38 saturates), exact
+    ties, NaN and Inf in row blocks and a NaN column block."""
     sv = inputs.special_values_bf16()
     rows = np.tile(sv, (128, 4)).astype(np.float32)         # 128 x 128
     rng = np.random.default_rng(0)
-    rows *= np.exp2(rng.integers(-20, 20, size=(128, 1))).astype(np.float32)
+    with np.errstate(over="ignore"):
+        rows *= np.exp2(rng.integers(-20, 20, size=(128, 1))).astype(np.float32)
     rows[5, :32] = 0.0
     rows[6, :32] = -0.0
     rows[7, 40] = np.nan
     rows[8, 70] = np.inf
     rows[9, 100] = -np.inf
     rows[64:96, 3] = np.nan                                  # a NaN column block
-    x = inputs.to_bf16(rows)
+    return inputs.to_bf16(rows)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+def test_special_values_and_edge_blocks(lib, fmt):
+    """Zero blocks (both signs), subnormal bf16, saturation, exact ties, NaN
+    and Inf blocks (scale 0xFF, zero codes)."""
+    x = _edge_blocks()
     for orient in ("row", "col", "dual"):
         for mode in ("floor", "ceil"):
             got, ref = run_both(lib, x, fmt, orient, mode)
+            check(got, ref, orient)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("rounding", ["sr", "sr4"])
+@pytest.mark.parametrize("had", [False, True])
+def test_stochastic_rounding_on_edge_blocks(lib, fmt, rounding, had):
+    """Stochastic rounding (one or four draws per generator call), with and
+    without the Hadamard, under both scale rules, on the edge blocks: zero
+    blocks keep their signs, saturating values round within [lo, max],
+    subnormal inputs and NaN/Inf blocks (scale 0xFF, zero codes; the
+    Hadamard spreads a NaN or Inf over its whole block) match the oracle."""
+    x = _edge_blocks()
+    for orient in ("row", "col", "dual"):
+        for mode in ("floor", "ceil"):
+            with np.errstate(invalid="ignore", over="ignore"):
+                got, ref = run_both(lib, x, fmt, orient, mode, rounding, had, 0x9E3779B97F4A7C15, 7)
             check(got, ref, orient)
 
 
@@ -272,23 +297,30 @@ def _sample_rows(n, k, seed):
 
 @pytest.mark.parametrize("fmt,gen,seed", [("e4m3", inputs.activations, 0), ("e5m2", inputs.gradients, 1)])
 @pytest.mark.parametrize("mode", ["floor", "ceil"])
-def test_full_size_dual_sampled(lib, fmt, gen, seed, mode):
-    """8192 x 4096 dual quantize in the launch configuration the benchmark
-    times; rows (row copy) and 32-row slabs (column copy) sampled."""
+@pytest.mark.parametrize("sf", ["mma", "canonical"])
+def test_full_size_dual_sampled(lib, fmt, gen, seed, mode, sf):
+    """8192 x 4096 dual quantize; with MMA-layout scales this is exactly the
+    launch the benchmark's headline times (all four of its runs).  Rows (row
+    copy) and 32-row slabs (column copy) are sampled; MMA-layout scales are
+    unpermuted to the canonical layout first."""
     x = gen(8192, 4096, seed=seed)
     dev = torch.device("cuda")
-    qr, sr, qc, sc = lib.mx_quantize(x.to(dev), fmt, "dual", mode)
+    qr, sr, qc, sc = lib.mx_quantize(x.to(dev), fmt, "dual", mode, sf_layout=sf)
+    sr, sc = np_(sr), np_(sc)
+    if sf == "mma":
+        sr = omx.sf_from_mma(sr, 8192, 4096 // 32)
+        sc = omx.sf_from_mma(sc, 4096, 8192 // 32)
     xv = f64(x)
     rows = _sample_rows(8192, 96, 1)
     ref = omx.quantize(xv[rows], FMTS[fmt], omx.ROW, MODE[mode])
     assert_bytes_equal(np_(qr)[rows], ref["q_row"], "q_row sample")
-    assert_bytes_equal(np_(sr)[rows], ref["s_row"], "s_row sample")
+    assert_bytes_equal(sr[rows], ref["s_row"], "s_row sample")
     slabs = _sample_rows(8192 // 32, 6, 2)
     for sl in slabs:
         r0 = sl * 32
         refc = omx.quantize(xv[r0:r0 + 32], FMTS[fmt], omx.COL, MODE[mode])
         assert_bytes_equal(np_(qc)[:, r0:r0 + 32], refc["q_col"], "q_col slab")
-        assert_bytes_equal(np_(sc)[:, sl:sl + 1], refc["s_col"], "s_col slab")
+        assert_bytes_equal(sc[:, sl:sl + 1], refc["s_col"], "s_col slab")
 
 
 def test_full_size_fp4_sr4_hadamard_sampled(lib):
@@ -346,6 +378,34 @@ def test_full_size_pertensor_one_step(lib):
     r = np_(ring)
     assert r[0] == np.float32(ramax)
     assert r[16] == np.float32(np.float64(np.float32(ramax)) / 448.0)
+
+
+def test_full_size_pertensor_sixteen_steps(lib):
+    """The per-tensor workload as the benchmark times it: 4096 x 14336,
+    step t quantizes base * 2^v_t (E4M3, dual) with the multiplier the
+    previous fold published (the ring's legacy slot) and folds into
+    hist[t % 16].  Each step: sampled x8 rows against the oracle, x8T equal
+    to the transpose of x8, and every ring slot equal to the oracle's host
+    fold (the tensor amax of step t is amax(base) * 2^v_t, exact)."""
+    dev = torch.device("cuda")
+    base = inputs.pertensor_base()
+    bv = f64(base)
+    amax0 = float(np.max(np.abs(bv)))
+    exps = inputs.pertensor_step_exponents(16, seed=3)
+    base_d = base.to(dev)
+    n = 16
+    ring = lib.ring_state_new(n, dev)
+    ring_ref = opt.ring_new(n)
+    rows = _sample_rows(4096, 8, 7)
+    for t, v in enumerate(exps):
+        xt = inputs.pertensor_step(base_d, v)
+        m = float(ring_ref[n + 1])
+        x8, x8T, _ = lib.quantize_dual(xt, ring[n + 1:n + 2], "e4m3", ring, t % n)
+        r8, _, _ = opt.quantize_pertensor(bv[rows] * 2.0 ** v, m, F.E4M3)
+        ring_ref = opt.ring_fold(ring_ref, amax0 * 2.0 ** v, t % n)
+        assert_bytes_equal(np_(x8)[rows], r8, f"x8 sample, step {t}")
+        assert torch.equal(x8T, x8.t().contiguous()), f"x8T, step {t}"
+        assert_bytes_equal(np_(ring).view(np.uint32), ring_ref.view(np.uint32), f"ring step {t}")
 
 
 def test_device_status_clean(lib):
