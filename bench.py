@@ -294,6 +294,12 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     fn = lambda: mxq.mm_fp8(x8, w8, X["one"], trans_b=True, bias=X["bias"], fmt="e4m3")
     n += extra_gemm_row(args, fn, timed, "fp8_pertensor_gemm_bias_8192x4096x4096", M, 4096, K, bf16, peak_src,
                         gemm_rows)
+    # the default layout of mm_fp8: b stored row-major [K][N] (the per-tensor
+    # quantizer's transposed copy of the [N][K] weight), read N-contiguous
+    w8kn = mxq.fp8_quantize_pertensor(W, X["one"], "e4m3", "col")[1]
+    fn = lambda: mxq.mm_fp8(x8, w8kn, X["one"], bias=X["bias"], fmt="e4m3")
+    n += extra_gemm_row(args, fn, timed, "fp8_pertensor_gemm_bias_kn_weight_8192x4096x4096", M, 4096, K, bf16,
+                        peak_src, gemm_rows)
     return n
 
 

@@ -6,8 +6,8 @@ current stream.  There is no fallback: if ``libmxq.so`` is missing or fails
 to load, every call raises.
 
 Entry points (same names as the C ABI):
-  mx_quantize, mx_dequantize, fp8_quantize_pertensor, mx_gemm, sf_to_mma,
-  last_device_status; plus ``quantize`` / ``quantize_dual`` with the
+  mx_quantize, mx_dequantize, fp8_quantize_pertensor, ring_fold, mx_gemm,
+  mx_gemm_mx_out, mm_fp8, sf_to_mma, last_device_status; plus ``quantize`` / ``quantize_dual`` with the
   argument order of AstrAI's fp8 adapter (astrai/extension/ops/fp8.py).
 """
 
@@ -57,17 +57,19 @@ def load() -> ctypes.CDLL:
     L.mxq_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, i32, i32, u64, u64, i32, vp, vp, vp, vp, vp]
     L.mxq_dequantize.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
     L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
+    L.fp8_ring_fold.argtypes = [vp, vp, i32, i32, f32, f32, vp]
     L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
     L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
     L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp]
-    L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
+    L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
     L.mxq_last_device_status.argtypes = [vp]
     L.mxq_strerror.argtypes = [i32]
     L.mxq_strerror.restype = ctypes.c_char_p
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
-    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed",
+    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
+                 "mxq_gemm_mixed",
                  "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32
@@ -251,6 +253,23 @@ def quantize_dual(x, scale, fmt="e4m3", ring_state=None, hist_idx=0, fp8_max=448
     return fp8_quantize_pertensor(x, scale, fmt, "dual", ring_state, hist_idx, fp8_max, pow2_margin)
 
 
+def ring_fold(amax: torch.Tensor, ring_state: torch.Tensor, hist_idx: int = 0, fp8_max: float = 448.0,
+              pow2_margin: float = 1.0) -> None:
+    """Fold a given tensor amax (a 1-element float32 device tensor) into the
+    ring and publish the next scale -- the fold fp8_quantize_pertensor runs
+    in its last block, for a tensor quantized in row shards whose amaxes were
+    MAX-reduced first (see ``shard.pertensor_step``)."""
+    if not isinstance(amax, torch.Tensor) or amax.dtype != torch.float32 or amax.numel() < 1:
+        raise ValueError("amax must be a float32 device tensor")
+    if (not isinstance(ring_state, torch.Tensor) or ring_state.dtype != torch.float32
+            or not ring_state.is_contiguous() or ring_state.numel() < 5):
+        raise ValueError("ring_state must be a contiguous float32 tensor of hist_len + 4 >= 5 elements")
+    _on_device(((amax, "amax"), (ring_state, "ring_state")), ring_state.device)
+    n = ring_state.numel() - 4
+    _call("fp8_ring_fold", ring_state.device, _ptr(amax), _ptr(ring_state), n, hist_idx, float(fp8_max),
+          float(pow2_margin))
+
+
 def ring_state_new(hist_len: int = 16, device="cuda") -> torch.Tensor:
     """Fresh ring [hist | scale | legacy | amax | done]: hist 0, scale 1, legacy 1, amax 0, done 0."""
     r = torch.zeros(hist_len + 4, dtype=torch.float32, device=device)
@@ -313,10 +332,12 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
     mm_fp8), bf16 result.  ``a``/``b`` hold FP8 codes (uint8 or a torch
     float8 dtype, which also gives the format), 2-D or 3-D (a batch axis
     broadcasts); op transposes the last two axes when the flag is set.
-    Views fold into the layout at zero copy as long as op(a) has K-contiguous
-    rows and op(b) K-contiguous columns (op(b) = w.t() for a row-major [N][K]
-    w); other layouts raise ValueError.  ``scale`` is a 1-element device
-    float32 tensor, ``bias`` a bf16 [N] vector."""
+    Transposed views are read in place, with no copy: op(a) may have
+    K-contiguous rows (a row-major [M][K]) or M-contiguous columns (the
+    transpose of a row-major [K][M]), op(b) K-contiguous columns (the
+    transpose of a row-major [N][K] weight) or N-contiguous rows (a
+    row-major [K][N]); any other layout raises ValueError.  ``scale`` is a
+    1-element device float32 tensor, ``bias`` a bf16 [N] vector."""
     if fmt is None:
         names = {getattr(torch, "float8_e4m3fn", None): "e4m3", getattr(torch, "float8_e5m2", None): "e5m2"}
         fmt = names.get(a.dtype, "e4m3")
@@ -329,10 +350,21 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
     if B.shape[-2] != K:
         raise ValueError(f"inner dimensions differ: {K} vs {B.shape[-2]}")
     N = B.shape[-1]
-    if A.stride(-1) != 1 or A.stride(-2) != K:
-        raise ValueError("op(a) must have K-contiguous rows (row-major [M][K])")
-    if B.stride(-2) != 1 or B.stride(-1) != K:
-        raise ValueError("op(b) must be the transposed view of a row-major [N][K] operand")
+    # storage of each operand: op(a) K-contiguous -> a row-major [M][K]
+    # (library trans_a 0), M-contiguous -> [K][M] (1); op(b) K-contiguous ->
+    # b row-major [N][K] (library trans_b 1), N-contiguous -> [K][N] (0)
+    if A.stride(-1) == 1 and A.stride(-2) == K:
+        ta = 0
+    elif A.stride(-2) == 1 and A.stride(-1) == M:
+        ta = 1
+    else:
+        raise ValueError("op(a) must be a row-major [M][K] matrix or the transpose of a row-major [K][M] one")
+    if B.stride(-2) == 1 and B.stride(-1) == K:
+        tb = 1
+    elif B.stride(-1) == 1 and B.stride(-2) == N:
+        tb = 0
+    else:
+        raise ValueError("op(b) must be a row-major [K][N] matrix or the transpose of a row-major [N][K] one")
     ba = A.shape[0] if A.dim() == 3 else 1
     bb = B.shape[0] if B.dim() == 3 else 1
     if ba > 1 and bb > 1 and ba != bb:
@@ -351,8 +383,8 @@ def mm_fp8(a: torch.Tensor, b: torch.Tensor, scale: torch.Tensor, trans_a: bool 
     _on_device(((a, "a"), (b, "b"), (scale, "scale"), (bias, "bias")), a.device)
     shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
     c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
-    _call("mxq_mm_fp8", a.device, _ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), f, _ptr(scale),
-          _ptr(bias), _ptr(c))
+    _call("mxq_mm_fp8", a.device, _ptr(A), _ptr(B), batch, M, N, K, int(ba > 1), int(bb > 1), ta, tb, f,
+          _ptr(scale), _ptr(bias), _ptr(c))
     return c
 
 

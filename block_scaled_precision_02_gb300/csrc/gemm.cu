@@ -98,6 +98,7 @@ struct Params {
   int mx_fmt, mx_ceil, mx_sf_mma;
   int* status;
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
+  int a_mn, b_mn;     // per-tensor kind: operand stored MN-major ([K][M] / [K][N] rows), else K-major
   uint32_t tx_bytes;  // bytes the loads of one stage complete on its "full" barrier (both CTAs of a pair)
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
@@ -245,15 +246,32 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_type, uint32_t b_ty
 
 // Instruction descriptor of the unscaled kind::f8f6f4 MMA: float32
 // accumulator (bits 4-5 = 1), A / B element types at bits 7-9 / 10-12,
-// K-major operands, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t instr_desc_f8(uint32_t a_type, uint32_t b_type, int n, int m) {
-  return (1u << 4) | (a_type << 7) | (b_type << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// A / B major-ness at bits 15 / 16 (0 K-major, 1 MN-major), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc_f8(uint32_t a_type, uint32_t b_type, int n, int m, uint32_t a_mn,
+                                                     uint32_t b_mn) {
+  return (1u << 4) | (a_type << 7) | (b_type << 10) | (a_mn << 15) | (b_mn << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+// Shared-memory descriptor of an operand tile and the descriptor step from
+// one 32-byte K slice to the next (16-byte units).  Both layouts are what a
+// TMA load with the 128-byte swizzle writes: K-major -- 128-byte rows along
+// K, one per M (N) index, 8-row groups 1024 bytes apart; MN-major -- 128-byte
+// rows along M (N), one per K index (the tile is 128 elements wide: a single
+// swizzle atom across), 8-row groups along K 1024 bytes apart, so a 32-deep
+// K slice is 32 rows = 4096 bytes.  An MN-major tile has one atom across,
+// so the atom stride across M (N) is never used; it is set to the 8-row
+// group stride as well.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr, int mn) {
+  return mn ? smem_desc(addr, 1024, 1024, 2) : smem_desc(addr, 16, 1024, 2);
+}
+__device__ __forceinline__ uint32_t k_slice_step(int mn) { return mn ? 256u : 2u; }
 
 template <int KIND>
 __device__ __forceinline__ uint32_t mma_idesc(const Params& p, int n, int m, int kk) {
-  if constexpr (KIND == KIND_F8) return instr_desc_f8(p.a_type, p.b_type, n, m);
+  if constexpr (KIND == KIND_F8)
+    return instr_desc_f8(p.a_type, p.b_type, n, m, static_cast<uint32_t>(p.a_mn), static_cast<uint32_t>(p.b_mn));
   else return instr_desc(p.a_type, p.b_type, n, m, KIND == KIND_MXF4 ? (kk & 1) * 2 : kk);
 }
 
@@ -567,16 +585,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       int u = 0;                                               // stage use counter
       for (int tile = blockIdx.x; tile < p.ntiles && !*abort_flag; tile += gridDim.x) {
         const TilePos tp = tile_pos(p, tile, BM, BN);
-        const int ar = tp.b * (p.a_batched ? p.M : 0) + tp.m0;   // operand rows
+        const int ar = tp.b * (p.a_batched ? p.M : 0) + tp.m0;   // operand rows (K-major)
         const int br = tp.b * (p.b_batched ? p.N : 0) + tp.n0;
+        const int ak = tp.b * (p.a_batched ? p.K : 0);           // first K row (MN-major)
+        const int bk = tp.b * (p.b_batched ? p.K : 0);
         for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
           const int s = u % STAGES;
           if (!mbar_wait(smem_u32(&empty[s]), ((u / STAGES) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, p.tx_bytes);
-          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
-          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
+          if (p.a_mn) tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, tp.m0, ak + kb * BKB);
+          else tma_load_2d(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
+          if (p.b_mn) tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, tp.n0, bk + kb * BKB);
+          else tma_load_2d(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
           if constexpr (C::SCALED) {
             const uint8_t* sfa_src = p.a_s + (static_cast<size_t>(tp.m0 / 128) * p.kb4) * 512;
             bulk_load_1d(smem_u32(sSFA + s * C::SFA_BYTES), sfa_src + kb * C::SFA_BYTES, C::SFA_BYTES, fb);
@@ -599,8 +621,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (lane == 0) {
       // Descriptors of stage 0, k-slice 0; every other (stage, slice) is a
       // plain add on the 14-bit start-address field (addresses stay < 256 KB).
-      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
-      const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      const uint64_t a_desc0 = operand_desc(smem_u32(sA), p.a_mn);
+      const uint64_t b_desc0 = operand_desc(smem_u32(sB), p.b_mn);
+      const uint32_t a_step = k_slice_step(p.a_mn), b_step = k_slice_step(p.b_mn);
       const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 0, 128, 0);
       const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
       uint32_t idesc[4];
@@ -638,7 +661,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             // the BN rows of B's chunk sit in BN / 32 consecutive columns.
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 4 * (BN / 128) * (kk >> 1) : sfb_t;
-            tc_mma<KIND>(tmem, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma<KIND>(tmem, ad + a_step * kk, bd + b_step * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit(smem_u32(&empty[s]));                       // stage free when these MMAs finish
         }
@@ -796,15 +819,20 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         const TilePos tp = tile_pos(p, tile, 256, 256);
         const int m0 = tp.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the product
         const int ar = tp.b * (p.a_batched ? p.M : 0) + m0;
-        const int br = tp.b * (p.b_batched ? p.N : 0) + tp.n0 + static_cast<int>(rank) * 128;
+        const int n0r = tp.n0 + static_cast<int>(rank) * 128;  // this CTA's half of B
+        const int br = tp.b * (p.b_batched ? p.N : 0) + n0r;
+        const int ak = tp.b * (p.a_batched ? p.K : 0);           // first K row (MN-major operands)
+        const int bk = tp.b * (p.b_batched ? p.K : 0);
         for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
           const int s = u % STAGES_P;
           if (!mbar_wait_suspend(smem_u32(&empty[s]), ((u / STAGES_P) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (rank == 0 && blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
           const uint32_t fb = cluster_map(smem_u32(&full[s]), 0);
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), p.tx_bytes);
-          tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
-          tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
+          if (p.a_mn) tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, m0, ak + kb * BKB);
+          else tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &map_a, fb, kb * BKB, ar);
+          if (p.b_mn) tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, n0r, bk + kb * BKB);
+          else tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &map_b, fb, kb * BKB, br);
           if constexpr (C::SCALED) {
             // scale maps: one 512-B chunk per row, chunk (rb, kc) at row rb * kb4 + kc
             tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &map_sfa, fb, 0, (m0 / 128) * p.kb4 + kb * C::SF_CHUNKS);
@@ -831,8 +859,9 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // (copied by warp 6, which runs ahead) -- or, unscaled, for the slot's
     // operands -- and issues the four MMAs only.
     if (lane == 0 && rank == 0) {
-      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
-      const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      const uint64_t a_desc0 = operand_desc(smem_u32(sA), p.a_mn);
+      const uint64_t b_desc0 = operand_desc(smem_u32(sB), p.b_mn);
+      const uint32_t a_step = k_slice_step(p.a_mn), b_step = k_slice_step(p.b_mn);
       uint32_t idesc[4];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) idesc[kk] = mma_idesc<KIND>(p, C::BN, 2 * BM, kk);
@@ -857,7 +886,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 8 * (kk >> 1) : sfb_t;
-            tc_mma_pair<KIND>(dacc, ad + 2 * kk, bd + 2 * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma_pair<KIND>(dacc, ad + a_step * kk, bd + b_step * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
           }
           tc_commit_pair_both(smem_u32(&empty[s]));            // stage free in both CTAs
           if (++s == STAGES_P) { s = 0; ph ^= 1; }
@@ -960,6 +989,7 @@ struct GemmArgs {
   int a_batched, b_batched;
   uint32_t a_type, b_type;
   int fp4;                        // both operands packed E2M1: kind::mxf4
+  int a_mn, b_mn;                 // per-tensor kind: operand stored [K][M] / [K][N] (MN-major)
   int a_u4, b_u4;                 // packed E2M1 beside an 8-bit operand (see encode_operand)
   int epi;
   void* c;                        // EPI_BF16 / EPI_FP32 output [batch * M][N]
@@ -999,6 +1029,8 @@ Params make_params(const GemmArgs& g, int tm, int tn, int64_t kbytes) {
   p.status = status_ptr();
   p.a_type = g.a_type;
   p.b_type = g.b_type;
+  p.a_mn = g.a_mn;
+  p.b_mn = g.b_mn;
   p.stall_u = take_test_stall(2) ? 0 : -1;
   return p;
 }
@@ -1034,6 +1066,26 @@ bool encode_operand(CUtensorMap* m, const void* q, bool u4, int64_t K, int64_t k
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// An MN-major FP8 operand's code map: the operand stored row-major as
+// [K][MN] (one row per K index, batch entries stacked), boxes of 128 bytes
+// along MN by 128 K rows, 128-byte swizzle -- the tile layout operand_desc
+// describes for MN-major operands.
+bool encode_operand_mn(CUtensorMap* m, const void* q, int64_t mn, uint64_t krows) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, mn, krows, mn, 128, mxq::gemm::BKB,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Both operand maps of a product (box_b: rows of B per tile when K-major).
+bool encode_operands(CUtensorMap* ma, CUtensorMap* mb, const GemmArgs& g, int64_t kbytes, uint32_t box_b) {
+  using namespace mxq::gemm;
+  const int64_t nba = g.a_batched ? g.batch : 1, nbb = g.b_batched ? g.batch : 1;
+  const bool a_ok = g.a_mn ? encode_operand_mn(ma, g.a_q, g.M, static_cast<uint64_t>(nba * g.K))
+                           : encode_operand(ma, g.a_q, g.a_u4, g.K, kbytes, static_cast<uint64_t>(nba * g.M), BM);
+  const bool b_ok = g.b_mn ? encode_operand_mn(mb, g.b_q, g.N, static_cast<uint64_t>(nbb * g.K))
+                           : encode_operand(mb, g.b_q, g.b_u4, g.K, kbytes, static_cast<uint64_t>(nbb * g.N), box_b);
+  return a_ok && b_ok;
+}
+
 // Transaction bytes of one operand tile: the widened E2M1 load completes the
 // packed bytes it reads (half its shared-memory footprint; the padding
 // slots are not written).
@@ -1045,10 +1097,7 @@ int launch(const GemmArgs& g, cudaStream_t st) {
   using Cf = Cfg<KIND, BN>;
   const int64_t kbytes = Cf::FP4 ? g.K / 2 : g.K;
   CUtensorMap ma, mb, mc;
-  const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
-  const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
-  if (!encode_operand(&ma, g.a_q, g.a_u4, g.K, kbytes, arows, BM)) return MXQ_ERR_CUDA;
-  if (!encode_operand(&mb, g.b_q, g.b_u4, g.K, kbytes, brows, BN)) return MXQ_ERR_CUDA;
+  if (!encode_operands(&ma, &mb, g, kbytes, BN)) return MXQ_ERR_CUDA;
   if (!encode_c(&mc, g)) return MXQ_ERR_CUDA;
   Params p = make_params(g, BM, BN, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
@@ -1107,10 +1156,7 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   const int64_t kbytes = Cf::FP4 ? g.K / 2 : g.K;
   const int64_t kb4 = g.K / 128;
   CUtensorMap ma, mb, msa, msb, mc;
-  const uint64_t arows = static_cast<uint64_t>((g.a_batched ? g.batch : 1) * g.M);
-  const uint64_t brows = static_cast<uint64_t>((g.b_batched ? g.batch : 1) * g.N);
-  if (!encode_operand(&ma, g.a_q, g.a_u4, g.K, kbytes, arows, BM)) return MXQ_ERR_CUDA;
-  if (!encode_operand(&mb, g.b_q, g.b_u4, g.K, kbytes, brows, 128)) return MXQ_ERR_CUDA;
+  if (!encode_operands(&ma, &mb, g, kbytes, 128)) return MXQ_ERR_CUDA;
   msa = CUtensorMap{};
   msb = CUtensorMap{};
   if (Cf::SCALED) {
@@ -1140,7 +1186,8 @@ int dispatch_out(const GemmArgs& g, cudaStream_t st) {
     const int pairs = max_pairs<KIND, MXOUT>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, Cf::SMEM, Cf::THREADS);
     if (pairs > 0) return launch_pair<KIND, MXOUT>(g, pairs, st);
   }
-  return (g.N % 256 == 0) ? launch<KIND, 256, MXOUT>(g, st) : launch<KIND, 128, MXOUT>(g, st);
+  // an MN-major B tile is one 128-element swizzle atom wide
+  return (g.N % 256 == 0 && !g.b_mn) ? launch<KIND, 256, MXOUT>(g, st) : launch<KIND, 128, MXOUT>(g, st);
 }
 
 // The MX outputs are separate kernels (row blocks only; with column
@@ -1254,13 +1301,14 @@ extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, c
 }
 
 extern "C" int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M, int64_t N, int64_t K,
-                          int a_batched, int b_batched, int fmt, const float* scale, const void* bias, void* c,
-                          void* stream) {
+                          int a_batched, int b_batched, int trans_a, int trans_b, int fmt, const float* scale,
+                          const void* bias, void* c, void* stream) {
   if (!a || !b || !scale || !c) return MXQ_ERR_BAD_ARG;
   if (fmt != MXQ_E4M3 && fmt != MXQ_E5M2) return fmt == MXQ_E2M1 ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
   if ((a_batched != 0 && a_batched != 1) || (b_batched != 0 && b_batched != 1)) return MXQ_ERR_BAD_ARG;
+  if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return MXQ_ERR_BAD_ARG;
   if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 128) return MXQ_ERR_BAD_SHAPE;
-  if (batch * M > (1ll << 31) - 256 || batch * N > (1ll << 31) - 256 || K > (1ll << 31) - 256)
+  if (batch * M > (1ll << 31) - 256 || batch * N > (1ll << 31) - 256 || batch * K > (1ll << 31) - 256)
     return MXQ_ERR_BAD_SHAPE;
   if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (bias && !aligned16(bias)) ||
       (reinterpret_cast<uintptr_t>(scale) & 3u))
@@ -1277,6 +1325,8 @@ extern "C" int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M
   g.b_batched = batch > 1 ? b_batched : 0;
   g.a_type = mma_type(fmt, false);
   g.b_type = mma_type(fmt, false);
+  g.a_mn = trans_a;               // a stored [K][M]: op(a) = a^T is M-contiguous
+  g.b_mn = !trans_b;              // b stored [K][N]: op(b) = b is N-contiguous
   g.epi = mxq::gemm::EPI_BF16;
   g.c = c;
   g.alpha = scale;

@@ -291,6 +291,30 @@ __device__ __forceinline__ void pertensor32(const uint32_t (&w)[16], float mult,
   for (int k = 0; k < 8; ++k) out[k] = fp8x4_rows<FMT>(w[2 * k], w[2 * k + 1], mm);
 }
 
+// The delayed-scaling fold (AstrAI fp8.py, commit message and quantize
+// docstring): ring = [hist[n] | scale | legacy | amax | done].  The tensor
+// amax goes to hist[hist_idx]; M = max(hist) (a NaN entry wins); when M is
+// finite and > 0 the next scale max(hist) / fp8_max / pow2_margin is
+// published as RN32(RN32(M / fp8_max) / margin), and legacy = RN32(1 / scale)
+// (the multiplier the next step passes in); the amax slot and the ticket
+// counter are reset to zero.  One thread runs it.
+__device__ __forceinline__ void fold_ring(volatile float* ring, int n, int hist_idx, float amax, float fp8_max,
+                                          float margin) {
+  ring[hist_idx] = amax;
+  float M = ring[0];
+  for (int k = 1; k < n; ++k) {
+    const float a = ring[k];
+    if (isnan(a) || a > M) M = a;
+  }
+  if (M > 0.f && isfinite(M)) {
+    const float sc = __fdiv_rn(__fdiv_rn(M, fp8_max), margin);
+    ring[n] = sc;
+    ring[n + 1] = __frcp_rn(sc);
+  }
+  ring[n + 2] = 0.f;
+  reinterpret_cast<volatile unsigned int*>(ring)[n + 3] = 0u;
+}
+
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int TC, int NSTG, int NOUT>
@@ -586,24 +610,24 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
           __threadfence();
           volatile float* vr = ring;
           const float amax = vr[n + 2];
-          vr[p.hist_idx] = amax;
-          float M = vr[0];
-          for (int k = 1; k < n; ++k) {
-            const float a = vr[k];
-            if (isnan(a) || a > M) M = a;
-          }
-          if (M > 0.f && isfinite(M)) {
-            const float sc = __fdiv_rn(__fdiv_rn(M, p.fp8_max), p.margin);
-            vr[n] = sc;
-            vr[n + 1] = __frcp_rn(sc);
-          }
           if (p.amax_out) *p.amax_out = amax;
-          vr[n + 2] = 0.f;
-          reinterpret_cast<volatile unsigned int*>(ring)[n + 3] = 0u;
+          fold_ring(vr, n, p.hist_idx, amax, p.fp8_max, p.margin);
           __threadfence();
         }
       }
     }
+  }
+}
+
+// The fold alone, of a given tensor amax: the step after the exchange of a
+// row-sharded per-tensor quantize (each shard's amax_out, then a MAX
+// reduction across the shards, then this fold on every replica of the ring).
+__global__ void ring_fold_kernel(const float* __restrict__ amax, float* ring, int n, int hist_idx, float fp8_max,
+                                 float margin) {
+  grid_dep_wait();
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    fold_ring(ring, n, hist_idx, *amax, fp8_max, margin);
+    __threadfence();
   }
 }
 
@@ -851,6 +875,16 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MXQ_ERR_CUDA;
   }
   return dispatch<true>(fmt, orient, mx, mr, mc, p, st);
+}
+
+extern "C" int fp8_ring_fold(const float* amax, float* ring_state, int hist_len, int hist_idx, float fp8_max,
+                             float pow2_margin, void* stream) {
+  if (!amax || !ring_state || hist_len < 1 || hist_idx < 0 || hist_idx >= hist_len) return MXQ_ERR_BAD_ARG;
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(ring_state) & 3u))
+    return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  return launch_pdl(ring_fold_kernel, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream), amax, ring_state,
+                    hist_len, hist_idx, fp8_max, pow2_margin);
 }
 
 extern "C" int mxq_dequantize(const void* q, const uint8_t* s, int64_t rows, int64_t cols, int fmt, int out_fp32,

@@ -101,9 +101,8 @@ extern "C" {
 /* ---- MX quantize ([MX] sections 1 and 4, gap sections 1-2; [FAF]) ----------
  * x        bf16 [rows][ld] (only the first cols of each row are read),
  *          16-byte aligned, ld % 8 == 0, ld >= cols.
- * rows, cols  positive multiples of 32 (an empty tensor is MXQ_ERR_BAD_SHAPE;
- *          rows % 128 and cols % 128 for SF_MMA;
- *          cols % 2... E2M1 needs even counts along the packed axis, given).
+ * rows, cols  positive multiples of 32 (an empty tensor is MXQ_ERR_BAD_SHAPE);
+ *          rows % 128 == 0 and cols % 128 == 0 for MXQ_SF_MMA.
  * fmt      MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1.
  * orient   MXQ_ROW | MXQ_COL | MXQ_DUAL.
  * scale_mode  MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL.
@@ -133,8 +132,8 @@ int mxq_dequantize(const void* q, const uint8_t* s, int64_t rows, int64_t cols,
                    int fmt, int out_fp32, void* out, void* stream);
 
 /* ---- per-tensor FP8 quantize with fused amax and delayed-scaling fold ([FP8])
- * x        bf16 [rows][cols], 16-byte aligned, cols % 8 == 0.  For COL/DUAL
- *          rows % 16 == 0 and cols % 16 == 0.
+ * x        bf16 [rows][cols], 16-byte aligned, cols % 16 == 0.  For COL/DUAL
+ *          also rows % 16 == 0.
  * scale    device float: the quantization multiplier m; x8 = RNE-saturating
  *          FP8 of RN32(x * m).  May alias ring_state[hist_len + 1].
  * fmt      MXQ_E4M3 | MXQ_E5M2.
@@ -157,6 +156,28 @@ int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
                            float* ring_state, int hist_len, int hist_idx,
                            float fp8_max, float pow2_margin, uint8_t* x8,
                            uint8_t* x8T, float* amax_out, void* stream);
+
+/* ---- delayed-scaling fold of a given tensor amax ([FP8] commit message:
+ * the fold takes the tensor's amax into the history and publishes the next
+ * scale) ---------------------------------------------------------------------
+ * The fold fp8_quantize_pertensor runs in its last block, as a call of its
+ * own, for a tensor quantized in row shards (one shard per GPU, each a
+ * multiple of 16 rows):
+ *   1. each shard: fp8_quantize_pertensor(x_shard, scale = &ring[hist_len+1],
+ *      ..., ring_state = NULL, ..., amax_out = a) -- a = the shard's amax;
+ *   2. a MAX all-reduce of the 4-byte a over the shards (e.g. NCCL);
+ *   3. each shard: fp8_ring_fold(a, ring, ...) on its own replica of the ring.
+ * Every replica then holds the ring a single whole-tensor call would leave.
+ * amax      device float: the tensor amax to fold (read by the kernel).
+ * ring_state device float[hist_len + 4], [hist | scale | legacy | amax | done]:
+ *           hist[hist_idx] = *amax; M = max(hist); if M is finite and > 0,
+ *           scale = RN32(RN32(M / fp8_max) / pow2_margin) and
+ *           legacy = RN32(1 / scale); amax and done are set to 0.
+ * hist_len >= 1, 0 <= hist_idx < hist_len; both pointers 4-byte aligned.
+ * One thread of the device does the fold, ordered on `stream`. */
+int fp8_ring_fold(const float* amax, float* ring_state, int hist_len,
+                  int hist_idx, float fp8_max, float pow2_margin,
+                  void* stream);
 
 /* ---- block-scaled GEMM ([MX] section 1: tensor cores consume X and q_i of
  * both operands, FP32 accumulation) -------------------------------------------
@@ -210,24 +231,29 @@ int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt,
                     void* stream);
 
 /* ---- per-tensor FP8 GEMM (AstrAI fp8.py, mm_fp8: "a @ b * scale (+ bias)",
- * scale the combined dequantization scale, bias added in the fp32 epilogue,
- * bf16 result) -------------------------------------------------------------------
+ * op() transposes when trans_a / trans_b is set, and a view that swaps the
+ * last two axes is read where it lies, with no copy; scale is the combined
+ * dequantization scale, bias is added in the fp32 epilogue, the result is
+ * bf16) --------------------------------------------------------------------------
  * c[i][m][n] = bf16_RNE( RN32( RN32(acc * scale) + bias[n] ) ), acc the
- * float32 tensor-core sum over k of dec(a[i][m][k]) * dec(b[i][n][k]).
- * a        FP8 codes, [batch][M][K] when a_batched, else [M][K] shared by
- *          every batch entry (K-contiguous rows).
- * b        FP8 codes, [batch][N][K] when b_batched, else [N][K] (the
- *          transposed view of a [K][N] operand: K-contiguous rows).
+ * float32 tensor-core sum over k of dec(op(a)[i][m][k]) * dec(op(b)[i][k][n]).
+ * a        FP8 codes, row-major: [batch][M][K] (trans_a == 0, op(a) = a) or
+ *          [batch][K][M] (trans_a == 1, op(a) = a^T); without a_batched one
+ *          matrix ([M][K] or [K][M]) serves every batch entry.
+ * b        FP8 codes, row-major: [batch][K][N] (trans_b == 0, op(b) = b) or
+ *          [batch][N][K] (trans_b == 1, op(b) = b^T, e.g. a weight stored
+ *          [out][in]); without b_batched one matrix serves every entry.
+ *          All four trans_a / trans_b combinations read the operands in
+ *          place (K-contiguous or M / N-contiguous rows).
  * fmt      MXQ_E4M3 | MXQ_E5M2 for both operands.
  * scale    device float (4-byte aligned), read by the kernel.
  * bias     NULL or device bf16 [N], 16-byte aligned.
  * c        bf16 [batch][M][N], 16-byte aligned.
- * batch >= 1; M, N, K multiples of 128.  Operands with M- or N-contiguous
- * rows are not taken (the per-tensor quantizer's transposed output gives the
- * K-contiguous copy). */
+ * batch >= 1; M, N, K multiples of 128. */
 int mxq_mm_fp8(const void* a, const void* b, int64_t batch, int64_t M,
-               int64_t N, int64_t K, int a_batched, int b_batched, int fmt,
-               const float* scale, const void* bias, void* c, void* stream);
+               int64_t N, int64_t K, int a_batched, int b_batched,
+               int trans_a, int trans_b, int fmt, const float* scale,
+               const void* bias, void* c, void* stream);
 
 /* ---- scale layout conversion ([FAF]) -----------------------------------------
  * Canonical scales s [rows][kb] -> MMA layout (rows % 128 == 0,

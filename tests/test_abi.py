@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "mxq_gemm", "mxq_gemm_mixed",
+    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
+              "mxq_gemm_mixed",
               "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
               "mxq_last_device_status", "mxq_strerror", "mxq_version"):
         assert n in names
@@ -119,12 +120,21 @@ def test_argument_checks_need_no_gpu(so):
     assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 100, 128, 1, 0, 0, 0, *row, None) == -2
 
     mm = so.mxq_mm_fp8
-    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 2, FAKE, None, FAKE, None) == -4   # E2M1
-    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, None, None, FAKE, None) == -1   # no scale
-    assert mm(FAKE, FAKE, 1, 128, 128, 128, 2, 0, 0, FAKE, None, FAKE, None) == -1   # batched flag
-    assert mm(FAKE, FAKE, 0, 128, 128, 128, 0, 0, 0, FAKE, None, FAKE, None) == -2   # batch 0
-    assert mm(FAKE, FAKE, 1, 100, 128, 128, 0, 0, 0, FAKE, None, FAKE, None) == -2
-    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, FAKE, ODD, FAKE, None) == -3   # bias alignment
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, 1, 2, FAKE, None, FAKE, None) == -4   # E2M1
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, 1, 0, None, None, FAKE, None) == -1   # no scale
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 2, 0, 0, 1, 0, FAKE, None, FAKE, None) == -1   # batched flag
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 2, 1, 0, FAKE, None, FAKE, None) == -1   # trans_a flag
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, -1, 0, FAKE, None, FAKE, None) == -1  # trans_b flag
+    assert mm(FAKE, FAKE, 0, 128, 128, 128, 0, 0, 0, 1, 0, FAKE, None, FAKE, None) == -2   # batch 0
+    assert mm(FAKE, FAKE, 1, 100, 128, 128, 0, 0, 1, 0, 0, FAKE, None, FAKE, None) == -2
+    assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, 0, 0, FAKE, ODD, FAKE, None) == -3   # bias alignment
+
+    rf = so.fp8_ring_fold
+    assert rf(None, FAKE, 16, 0, 448.0, 1.0, None) == -1           # no amax
+    assert rf(FAKE, None, 16, 0, 448.0, 1.0, None) == -1           # no ring
+    assert rf(FAKE, FAKE, 16, 16, 448.0, 1.0, None) == -1          # hist_idx out of range
+    assert rf(FAKE, FAKE, 0, 0, 448.0, 1.0, None) == -1            # empty history
+    assert rf(ctypes.c_void_p(0x10002), FAKE, 16, 0, 448.0, 1.0, None) == -3
 
     assert so.mxq_dequantize(FAKE, FAKE, 64, 48, 0, 1, FAKE, None) == -2
     assert so.mxq_sf_to_mma(FAKE, 100, 4, FAKE, None) == -2

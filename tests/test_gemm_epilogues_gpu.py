@@ -19,7 +19,7 @@ from block_scaled_precision_02_gb300 import inputs
 from oracle import formats as F
 from oracle import gemm as og
 from oracle import mx as omx
-from tests.helpers import assert_bytes_equal, f64
+from tests.helpers import assert_bytes_equal, f64, np_
 
 pytestmark = pytest.mark.gpu
 
@@ -254,18 +254,81 @@ def test_mm_fp8_more_tiles_than_pairs(lib):
     assert og.gate_error(c.float().cpu().numpy().astype(np.float64), ref) <= 2e-3
 
 
-def test_mm_fp8_views_fold_and_bad_layouts_raise(lib):
+def _stored(x, trans):
+    """The operand as the library reads it: x itself, or the transpose of a
+    row-major copy of x^T (the same matrix, other-axis contiguous)."""
+    if not trans:
+        return t(x)
+    return t(np.ascontiguousarray(np.swapaxes(x, -1, -2))).transpose(-1, -2)
+
+
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("mnk", [(128, 384, 256), (256, 512, 512), (384, 256, 384)])
+def test_mm_fp8_every_layout_one_hot_exact(lib, a_mn, b_mn, mnk):
+    """Operands K-contiguous or M/N-contiguous (a row-major [K][M] a used as
+    a^T, a row-major [K][N] b), read in place: one-hot rows of op(a) pick
+    columns of op(b) exactly, on the CTA-pair kernel (M, N multiples of 256)
+    and the single-CTA one (the other shapes)."""
+    M, N, K = mnk
+    rng = np.random.default_rng(31)
+    a8 = np.zeros((M, K), dtype=np.uint8)
+    a8[np.arange(M), rng.integers(0, K, M)] = fp8_codes(np.array([1.0]), "e4m3")[0]
+    b8 = fp8_codes(rng.standard_normal((N, K)) * 8, "e4m3")            # logical B^T [N][K]
+    scale = torch.tensor([0.5], dtype=torch.float32, device=dev)
+    A = _stored(a8, a_mn)                                                  # op(a) [M][K]
+    B = _stored(b8, b_mn).transpose(-1, -2)                            # op(b) [K][N]
+    assert (A.stride(-2) == 1) == a_mn and (B.stride(-1) == 1) == b_mn
+    c = lib.mm_fp8(A, B, scale, fmt="e4m3")
+    ref = og.mm_fp8_reference(a8, b8, F.E4M3, 0.5)
+    assert np.array_equal(c.float().cpu().numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("shape,a_batched,b_batched", [((2, 256, 512, 384), True, False),
+                                                       ((3, 256, 256, 256), True, True),
+                                                       ((2, 128, 256, 256), False, True),
+                                                       ((1, 512, 768, 1024), True, True)])
+def test_mm_fp8_every_layout_gate(lib, fmt, a_mn, b_mn, shape, a_batched, b_batched):
+    """Random FP8 operands in all four layouts, batched or broadcast, with
+    bias: within the GEMM gate of the float64 product."""
+    batch, M, N, K = shape
+    rng = np.random.default_rng(32)
+    a8 = fp8_codes(rng.standard_normal((batch, M, K) if a_batched else (M, K)), fmt)
+    b8 = fp8_codes(rng.standard_normal((batch, N, K) if b_batched else (N, K)) * 2, fmt)
+    bias = inputs.to_bf16(rng.standard_normal(N).astype(np.float32))
+    sc = np.float32(0.0371)
+    scale = torch.tensor([sc], dtype=torch.float32, device=dev)
+    A = _stored(a8, a_mn)
+    B = _stored(b8, b_mn).transpose(-1, -2)
+    c = lib.mm_fp8(A, B, scale, bias=bias.to(dev), fmt=fmt)
+    a_full = np.broadcast_to(a8, (batch, M, K))
+    b_full = np.broadcast_to(b8, (batch, N, K))
+    ref = og.mm_fp8_reference(a_full, b_full, FMTS[fmt], float(sc), f64(bias))
+    got = c.float().cpu().numpy().astype(np.float64).reshape(ref.shape)
+    assert og.gate_error(got, ref) <= 2e-3
+
+
+def test_mm_fp8_trans_flags_and_bad_layouts(lib):
+    """trans_a / trans_b transpose the stored operands (AstrAI mm_fp8
+    semantics); a strided slice that is neither layout raises."""
     rng = np.random.default_rng(25)
-    a8 = t(fp8_codes(rng.standard_normal((256, 256)), "e4m3"))
-    w8 = t(fp8_codes(rng.standard_normal((256, 256)), "e4m3"))
+    a8 = t(fp8_codes(rng.standard_normal((256, 512)), "e4m3"))             # [M][K]
+    w8 = t(fp8_codes(rng.standard_normal((384, 512)), "e4m3"))             # [N][K]
     scale = torch.tensor([1.0], dtype=torch.float32, device=dev)
     c1 = lib.mm_fp8(a8, w8, scale, trans_b=True)
     c2 = lib.mm_fp8(a8, w8.t(), scale)
+    c3 = lib.mm_fp8(a8, w8.t().contiguous(), scale)                        # b stored [K][N]
+    c4 = lib.mm_fp8(a8.t().contiguous(), w8.t().contiguous(), scale, trans_a=True)
     assert torch.equal(c1, c2)
+    ref = og.mm_fp8_reference(np_(a8), np_(w8), F.E4M3, 1.0)
+    for c in (c1, c3, c4):
+        assert og.gate_error(c.float().cpu().numpy().astype(np.float64), ref) <= 2e-3
+    big = t(fp8_codes(rng.standard_normal((256, 1024)), "e4m3"))
     with pytest.raises(ValueError):
-        lib.mm_fp8(a8, w8, scale)                                # row-major [K][N] b: N-contiguous
-    with pytest.raises(ValueError):
-        lib.mm_fp8(a8, w8, scale, trans_a=True, trans_b=True)   # op(a) M-contiguous
+        lib.mm_fp8(big[:, ::2], w8, scale, trans_b=True)                   # every other column
 
 
 # ---------------------------------------------------------------- full sizes, sampled
