@@ -99,6 +99,7 @@ struct Params {
   int* status;
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
   int a_mn, b_mn;     // per-tensor kind: operand stored MN-major ([K][M] / [K][N] rows), else K-major
+  int m_fast;         // tile order: M index fastest (A resident in L2), else N fastest
   uint32_t tx_bytes;  // bytes the loads of one stage complete on its "full" barrier (both CTAs of a pair)
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
@@ -107,9 +108,14 @@ struct Params {
 struct TilePos {
   int b, m0, n0;
 };
+// Tiles run in waves of consecutive indices.  With m_fast the index walks
+// down M first, so a wave covers every M tile of a few N columns and A stays
+// in L2 while B streams through once; otherwise N runs first and B stays.
+// The host picks the order that keeps the smaller operand resident.
 __device__ __forceinline__ TilePos tile_pos(const Params& p, int tile, int tm, int tn) {
   const int per = p.tiles_m * p.tiles_n;
   const int b = tile / per, r = tile - b * per;
+  if (p.m_fast) return {b, (r % p.tiles_m) * tm, (r / p.tiles_m) * tn};
   return {b, (r / p.tiles_n) * tm, (r % p.tiles_n) * tn};
 }
 
@@ -1031,6 +1037,8 @@ Params make_params(const GemmArgs& g, int tm, int tn, int64_t kbytes) {
   p.b_type = g.b_type;
   p.a_mn = g.a_mn;
   p.b_mn = g.b_mn;
+  // keep the operand with fewer rows (the smaller one) resident in L2
+  p.m_fast = (g.a_batched == g.b_batched) && g.M < g.N;
   p.stall_u = take_test_stall(2) ? 0 : -1;
   return p;
 }

@@ -13,18 +13,23 @@
 // 32-point Hadamard, scale layout written for its consumer).
 //
 // Design (one kernel shape for every mode):
-//  * The tensor is cut into 128 x 128 bf16 tiles.  A persistent grid of two
-//    256-thread CTAs per SM walks the tiles; each tile arrives by two TMA
-//    loads (128 rows x 64 columns, 128-byte swizzle) into a two-stage ring,
-//    so HBM reads of the next tiles overlap the work on the current one.
-//  * Row pass: 16 lanes per row, 8 bf16 per lane; a 1x32 block is 4 lanes,
-//    its amax is two xor-shuffles.  Column pass: one lane per two columns
-//    reads 32 rows with 4-byte shared loads (conflict-free) and owns two
-//    32x1 blocks entirely in registers.
-//  * Codes are staged in shared memory and leave by TMA stores (the column
-//    copy is written transposed, so its rows are 128 contiguous bytes of
-//    the tile); scales leave as 4-byte or 16-byte stores in the requested
-//    layout (canonical, or the GEMM's 512-byte tensor-core chunks).
+//  * The tensor is cut into 128-row x 64-column bf16 tiles (16 KiB).  A
+//    persistent grid of 256-thread CTAs (as many per SM as fit) walks the
+//    tiles; each tile arrives by one TMA load (128-byte swizzle) into a ring
+//    of NSTG stages, so HBM reads of the next tiles overlap the work on the
+//    current one.
+//  * Every warp owns a fixed part of each tile and runs on its own: it waits
+//    for the tile's stage, quantizes its part, stages its codes in its own
+//    shared-memory buffers and issues its own TMA store.  There is no barrier
+//    across warps in the loop.  The last warp to finish reading a stage (a
+//    shared-memory counter tells which) issues the stage's next load.
+//  * Dual orientation: warps 0-3 take 32 rows each (one lane per row, both
+//    1 x 32 blocks of the row); warps 4-7 take a 32-row band each (one lane
+//    per two adjacent columns, two 32 x 1 blocks in registers).  Row only:
+//    eight warps of 16 rows (one block per lane).  Column only: warps 0-3.
+//  * The column copy is staged transposed, so it leaves as rows of q_col.
+//    Scales leave from the lanes that computed them, in the requested layout
+//    (canonical, or the GEMM's 512-byte tensor-core chunks).
 //  * One HBM read of x produces every requested output.
 #include <algorithm>
 
@@ -32,35 +37,29 @@
 
 namespace mxq {
 
-// Tile shape of the quantizers: 128 rows x TC columns of bf16, NSTG input
-// stages per CTA (build-time knobs; the defaults are the measured best).
-#ifndef MXQ_QUANT_TC
-#define MXQ_QUANT_TC 64
-#endif
+// Pipeline depth of the quantizers: NSTG input stages per CTA and NOUT
+// staging buffers per warp (2 lets a warp stage a tile while the bulk store
+// of its previous tile still reads shared memory).  Build-time knobs; the
+// defaults are the measured best.
 #ifndef MXQ_QUANT_NST
 #define MXQ_QUANT_NST 3
 #endif
-// staging buffers for the outgoing code tiles: 2 lets a tile be staged while
-// the previous tile's bulk stores are still reading shared memory
 #ifndef MXQ_QUANT_STG
 #define MXQ_QUANT_STG 2
 #endif
 constexpr int TR = 128;                     // tile rows
 constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
 
-template <int TC, int NSTG, int NSTAGE_OUT, bool EXTRA>
+template <int NSTG, int NOUT, bool EXTRA>
 struct TileCfg {
-  static_assert(TC == 64 || TC == 128, "tile width");
-  static constexpr int THREADS = TC * 4;            // one warp per 8 tile columns
+  static constexpr int TC = 64;                     // tile columns
+  static constexpr int THREADS = 256;
   static constexpr int NW = THREADS / 32;
-  static constexpr int IN_BYTES = TR * TC * 2;
-  static constexpr int ROW_BLOCKS = TC / 32;        // 1x32 blocks per tile row
-  static constexpr int ROW_TASKS = 4 * ROW_BLOCKS;  // 32 rows x one block each (= NW)
-  static constexpr int COL_TASKS = TC / 16;         // 64 columns x 32 rows each (= NW / 2)
+  static constexpr int IN_BYTES = TR * TC * 2;      // one stage: 128 x 64 bf16
+  static constexpr int STG = 2048;                  // one staging buffer of one warp
+  static constexpr int SMEM = NSTG * IN_BYTES + NW * NOUT * STG + 256 + 1024;
   // resident CTAs per SM the registers are budgeted for
-  static constexpr int SMEM_KB = (NSTG * TR * TC * 2 + NSTAGE_OUT * 2 * TR * TC) / 1024;   // approx.
-  static constexpr int MIN_BLOCKS = EXTRA ? (TC == 128 ? 1 : 2)
-                                          : (TC == 128 ? 2 : (SMEM_KB <= 50 ? 4 : (SMEM_KB <= 70 ? 3 : 2)));
+  static constexpr int MIN_BLOCKS = EXTRA ? 2 : (SMEM <= 70 * 1024 ? 3 : 2);
 };
 
 // 16-byte chunk index after the TMA swizzle of a staged row of `pitch`
@@ -317,175 +316,200 @@ __device__ __forceinline__ void fold_ring(volatile float* ring, int n, int hist_
 
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
-template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int TC, int NSTG, int NOUT>
-__global__ void __launch_bounds__(TileCfg<TC, NSTG, NOUT, EXTRA>::THREADS, TileCfg<TC, NSTG, NOUT, EXTRA>::MIN_BLOCKS)
+template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT>
+__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
                    const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
-  using T = TileCfg<TC, NSTG, NOUT, EXTRA>;
+  using T = TileCfg<NSTG, NOUT, EXTRA>;
+  constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
+  constexpr bool DUAL = DO_ROW && DO_COL;
   constexpr bool FP4 = (FMT == MXQ_E2M1);
-  constexpr int QBR = FP4 ? TC / 2 : TC;            // code bytes per staged tile row
-  constexpr int QBC = FP4 ? TR / 2 : TR;            // code bytes per staged tile column
-  constexpr int ROWSTG = (TR * QBR + 1023) & ~1023;
-  constexpr int COLSTG = (TC * QBC + 1023) & ~1023;
+  constexpr int QBR = FP4 ? TC / 2 : TC;            // code bytes per tile row
+  constexpr int QBW = FP4 ? 16 : 32;                // code bytes per column per 32-row band
+  constexpr int RR = DUAL ? 32 : 16;                // rows of a row warp
+  constexpr int BPL = DUAL ? 2 : 1;                 // 1 x 32 blocks per lane of a row warp
+  constexpr int ROW_WARPS = DO_ROW ? (DUAL ? 4 : 8) : 0;
+  constexpr int ACTIVE = ROW_WARPS + (DO_COL ? 4 : 0);   // warps that read every stage
+  static_assert(RR * QBR <= T::STG && 64 * QBW <= T::STG, "staging buffer");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* in_s = smem;
-  uint8_t* qrow_base = in_s + NSTG * T::IN_BYTES;       // NOUT row staging tiles
-  uint8_t* qcol_base = qrow_base + NOUT * ROWSTG;         // NOUT column staging tiles
-  uint8_t* scr_s = qcol_base + NOUT * COLSTG;   // [128 rows][ROW_BLOCKS] scale bytes
-  uint8_t* scc_s = scr_s + 512;          // [TC columns][4] scale bytes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(scc_s + 512);
-  uint32_t* red = reinterpret_cast<uint32_t*>(bars + NSTG);
+  uint8_t* in_s = smem;                                   // NSTG x 16 KiB stages
+  uint8_t* stg_s = in_s + NSTG * T::IN_BYTES;             // per warp NOUT staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + T::NW * NOUT * T::STG);   // full[NSTG]
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(bars + NSTG);       // readers done with each stage
+  int* last_use = reinterpret_cast<int*>(cnt + NSTG);             // latest load issued into each stage
+  uint32_t* red = reinterpret_cast<uint32_t*>(last_use + NSTG);   // per-warp amax (per-tensor)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + T::NW);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t signs = (EXTRA && p.hadamard) ? hadamard_sign_mask(p.had_k0, p.had_k1) : 0u;
 
-  if (tid == 0) {
-    for (int s = 0; s < NSTG; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
-    prefetch_tensormap(&map_x);
-    if (DO_ROW) prefetch_tensormap(&map_qrow);
-    if (DO_COL) prefetch_tensormap(&map_qcol);
-  }
-  __syncthreads();
-  grid_dep_launch();
-  grid_dep_wait();                 // before any global-memory access
-  const float mult = PERTENSOR ? *p.scale : 1.0f;
-
-  int issued = 0;
-  auto issue = [&](int i) {  // thread 0 only
+  // Load of this CTA's tile i into its stage (issued by one thread).
+  auto issue = [&](int i) {
     const int tile = blockIdx.x + i * gridDim.x;
     if (tile == p.stall_tile) return;      // test hook: leave this stage's phase incomplete
     const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
     const uint32_t bar = smem_u32(&bars[i % NSTG]);
-    uint8_t* dst = in_s + (i % NSTG) * T::IN_BYTES;
+    last_use[i % NSTG] = i;
     mbar_arrive_expect_tx(bar, T::IN_BYTES);
-#pragma unroll
-    for (int h = 0; h < TC / 64; ++h) tma_load_2d(smem_u32(dst + h * BOX_BYTES), &map_x, bar, c0 + 64 * h, r0);
+    tma_load_2d(smem_u32(in_s + (i % NSTG) * T::IN_BYTES), &map_x, bar, c0, r0);
   };
+
   if (tid == 0) {
+    for (int s = 0; s < NSTG; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      cnt[s] = 0;
+      last_use[s] = -1;
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&map_x);
+    if (DO_ROW) prefetch_tensormap(&map_qrow);
+    if (DO_COL) prefetch_tensormap(&map_qcol);
+    // The first tiles' input into L2 while the previous kernel in the stream
+    // may still be finishing.  L2 is where the GPU's memory is coherent: a
+    // write of that kernel that lands later updates the prefetched line, and
+    // the loads below are issued only after grid_dep_wait, so they see it.
     for (int i = 0; i < NSTG; ++i) {
-      if (blockIdx.x + i * gridDim.x < p.ntiles) { issue(i); issued = i + 1; }
+      const int tile = blockIdx.x + i * gridDim.x;
+      if (tile < p.ntiles) tma_prefetch_2d(&map_x, (tile % p.tiles_c) * TC, (tile / p.tiles_c) * TR);
     }
   }
-
-  // Work split: row tasks (32 rows x one 32-column block, one lane per 1x32
-  // block) and column tasks (64 columns x 32 rows, one lane per two 32x1
-  // blocks).  Dual: the first half of the warps take two row tasks each,
-  // the second half one column task each, so both passes run side by side.
-  int row_task0 = -1, row_task1 = -1, col_task = -1;
-  if constexpr (DO_ROW && DO_COL) {
-    if (warp < T::NW / 2) { row_task0 = warp; row_task1 = warp + T::NW / 2; } else { col_task = warp - T::NW / 2; }
-  } else if constexpr (DO_ROW) {
-    row_task0 = warp;
-  } else {
-    if (warp < T::COL_TASKS) col_task = warp;
+  __syncthreads();
+  grid_dep_launch();
+  grid_dep_wait();                 // before any other global-memory access
+  const float mult = PERTENSOR ? *p.scale : 1.0f;
+  if (tid == 0) {
+    for (int i = 0; i < NSTG; ++i)
+      if (blockIdx.x + i * gridDim.x < p.ntiles) issue(i);
   }
+
+  // This warp's part of every tile.
+  const bool row_warp = warp < ROW_WARPS;
+  const int col_band = DO_COL ? (DUAL ? warp - 4 : (DO_ROW ? -1 : warp)) : -1;
+  const bool col_warp = DO_COL && col_band >= 0 && col_band < 4;
+  const int ro = row_warp ? warp * RR : 0;           // first tile row of a row warp
 
   uint32_t amax_acc = 0;   // per-tensor: running max of |x| bits
-  bool aborted = false;
-  int i = 0;
-  for (;; ++i) {
-    const int tile = blockIdx.x + i * gridDim.x;
-    if (tile >= p.ntiles) break;
-    const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
-    const int s = i % NSTG;
-    const uint32_t full_bar = smem_u32(&bars[s]);
-    const uint32_t parity = (i / NSTG) & 1;
-    // Thread 0 alone waits for the tile's TMA loads (bounded) and for the
-    // bulk stores that last used this tile's staging buffers to have read
-    // them out (each tile commits one store group); the rest of the CTA
-    // waits at the barrier instead of spinning.
-    bool ok = true;
-    if (tid == 0) {
-      ok = mbar_wait(full_bar, parity, p.status);
-      if constexpr (NOUT == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      else bulk_wait_read_all();
-    }
-    uint8_t* qrow_s = qrow_base + (i % NOUT) * ROWSTG;
-    uint8_t* qcol_s = qcol_base + (i % NOUT) * COLSTG;
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    // each thread observes the completed phase itself (acquire); it has
-    // completed, so this returns at once
-    if (!mbar_try_wait(full_bar, parity)) (void)mbar_wait(full_bar, parity, p.status);
-    const uint8_t* in = in_s + s * T::IN_BYTES;
-
-    // ------------------------------------------------------------ row pass
-    // Shared loads are 16-byte and conflict-free: the TMA 128-byte swizzle
-    // puts the 8 rows of a load phase in 8 different bank groups.
-    if constexpr (DO_ROW) {
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int task = t ? row_task1 : row_task0;
-        if (task < 0) continue;
-        const int b = task % T::ROW_BLOCKS;
-        const int r = (task / T::ROW_BLOCKS) * 32 + lane;
-        const uint8_t* src = in + (b >> 1) * BOX_BYTES + r * 128;
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 q = *reinterpret_cast<const uint4*>(src + ((((b & 1) * 4 + k) ^ (r & 7)) << 4));
-          w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
-        }
-        uint32_t out[8];
-        if constexpr (PERTENSOR) {
-          amax_acc = max(amax_acc, amax_bf16x32(w));
-          pertensor32<FMT>(w, mult, out);
-        } else if constexpr (!EXTRA) {
-          const uint32_t ab = amax_bf16x32(w);
-          const bool bad = ab >= 0x7F800000u;
-          const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
-          rne_words16<FMT>(w, exp2_neg(e), out);
-          zero_if_bad(bad, out);
-          scr_s[r * T::ROW_BLOCKS + b] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
-        } else {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) { v[2 * j] = bf16lo(w[j]); v[2 * j + 1] = bf16hi(w[j]); }
-          uint32_t ab;
-          if (p.hadamard) {
-            hadamard32(v, signs);
-            ab = 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ab = max(ab, absbits(v[j]));
-          } else {
-            ab = amax_bf16x32(w);
-          }
-          const uint64_t idx0 = static_cast<uint64_t>(r0 + r) * static_cast<uint64_t>(p.cols) + (c0 + 32 * b);
-          const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, 1, out);
-          scr_s[r * T::ROW_BLOCKS + b] = static_cast<uint8_t>(sc);
-        }
-        if constexpr (FP4) {
-          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-        } else {
-          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, 2 * b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-          *reinterpret_cast<uint4*>(qrow_s + r * QBR + (swz(r, 2 * b + 1, QBR) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
-        }
+  if (row_warp || col_warp) {
+    for (int i = 0;; ++i) {
+      const int tile = blockIdx.x + i * gridDim.x;
+      if (tile >= p.ntiles || *abort_flag) break;
+      const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
+      const int s = i % NSTG;
+      if (!mbar_wait(smem_u32(&bars[s]), (i / NSTG) & 1, p.status)) {
+        *abort_flag = 1;
+        break;
       }
-    }
+      const uint8_t* in = in_s + s * T::IN_BYTES;
+      uint8_t* stg = stg_s + (warp * NOUT + i % NOUT) * T::STG;
+      // this buffer was last read by the bulk store of tile i - NOUT
+      if (lane == 0) {
+        if constexpr (NOUT == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else bulk_wait_read_all();
+      }
+      __syncwarp();
 
-    // ------------------------------------------------------------ column pass
-    // 4-byte shared loads: a warp reads 128 contiguous bytes of a row.
-    if constexpr (DO_COL) {
-      if (col_task >= 0) {
-        const int hh = col_task % (TC / 64), rb = col_task / (TC / 64);
+      if (row_warp) {
+        // ---------------------------------------------------------- row blocks
+        // 16-byte shared loads, conflict-free: the 128-byte swizzle puts the
+        // 8 rows of a load phase in 8 different bank groups.
+        const int r = lane % RR, row = ro + r;
+        uint32_t sc2 = 0;
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) {
+          const int b = (lane / RR) * BPL + j;
+          const uint8_t* src = in + row * 128;
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 q = *reinterpret_cast<const uint4*>(src + (((b * 4 + k) ^ (row & 7)) << 4));
+            w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
+          }
+          uint32_t out[8];
+          uint32_t sc = 0;
+          if constexpr (PERTENSOR) {
+            amax_acc = max(amax_acc, amax_bf16x32(w));
+            pertensor32<FMT>(w, mult, out);
+          } else if constexpr (!EXTRA) {
+            const uint32_t ab = amax_bf16x32(w);
+            const bool bad = ab >= 0x7F800000u;
+            const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
+            rne_words16<FMT>(w, exp2_neg(e), out);
+            zero_if_bad(bad, out);
+            sc = bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+          } else {
+            float v[32];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) { v[2 * q] = bf16lo(w[q]); v[2 * q + 1] = bf16hi(w[q]); }
+            uint32_t ab;
+            if (p.hadamard) {
+              hadamard32(v, signs);
+              ab = 0;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) ab = max(ab, absbits(v[q]));
+            } else {
+              ab = amax_bf16x32(w);
+            }
+            const uint64_t idx0 = static_cast<uint64_t>(r0 + row) * static_cast<uint64_t>(p.cols) + (c0 + 32 * b);
+            sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, 1, out);
+          }
+          sc2 |= sc << (8 * j);
+          if constexpr (FP4) {
+            *reinterpret_cast<uint4*>(stg + r * QBR + (swz(r, b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+          } else {
+            *reinterpret_cast<uint4*>(stg + r * QBR + (swz(r, 2 * b, QBR) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(stg + r * QBR + (swz(r, 2 * b + 1, QBR) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_qrow, smem_u32(stg), FP4 ? c0 / 2 : c0, r0 + ro);
+          bulk_commit();
+        }
+        // row scales: the lane's BPL bytes (blocks b0 .. b0 + BPL - 1 of its row)
+        if constexpr (!PERTENSOR) {
+          const int b0 = c0 / 32 + (lane / RR) * BPL, kb = p.cols / 32;
+          if (r0 + row < p.rows && b0 < kb) {
+            uint8_t* dst;
+            bool vec = BPL == 2;
+            if (p.sf_mma) {   // full tiles only (rows, cols % 128 == 0)
+              dst = p.s_row + (static_cast<size_t>(r0 / 128) * (p.cols / 128) + c0 / 128) * 512 + (row & 31) * 16 +
+                    ((row >> 5) & 3) * 4 + (b0 & 3);
+            } else {
+              dst = p.s_row + static_cast<size_t>(r0 + row) * kb + b0;
+              vec = vec && (kb % 2) == 0 && b0 + 2 <= kb;
+            }
+            if (vec) {
+              *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(sc2);
+            } else {
+              for (int j = 0; j < BPL && b0 + j < kb; ++j) dst[j] = static_cast<uint8_t>(sc2 >> (8 * j));
+            }
+          }
+        }
+      } else {
+        // ---------------------------------------------------------- column blocks
+        // 4-byte shared loads: a warp reads 128 contiguous bytes of a row.
+        const int rb = col_band;
         const int chk = lane >> 2, wb = (lane & 3) * 4;
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int row = rb * 32 + k;
-          w[k] = *reinterpret_cast<const uint32_t*>(in + hh * BOX_BYTES + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
+          w[k] = *reinterpret_cast<const uint32_t*>(in + row * 128 + ((chk ^ (k & 7)) << 4) + wb);
         }
         uint32_t m2 = 0;                       // packed amax of both columns
 #pragma unroll
         for (int k = 0; k < 32; ++k) m2 = hmax2_abs(m2, w[k]);
         m2 = amax_halves(m2);
+        uint32_t scb[2] = {0u, 0u};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int cl = hh * 64 + 2 * lane + half;       // tile column
+          const int cl = 2 * lane + half;       // tile column = staged row
           uint32_t out[8];
           const uint32_t abw = half ? (m2 & 0xFFFF0000u) : (m2 << 16);
           if constexpr (PERTENSOR) {
@@ -496,7 +520,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
             const int e = scale_exp<FMT>(bad ? 0u : abw, p.ceil_mode);
             rne_col32<FMT>(w, half, exp2_neg(e), out);
             zero_if_bad(bad, out);
-            scc_s[cl * 4 + rb] = bad ? 0xFFu : static_cast<uint8_t>(e + 127);
+            scb[half] = bad ? 0xFFu : static_cast<uint32_t>(e + 127);
           } else {
             float v[32];
 #pragma unroll
@@ -509,84 +533,60 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
               for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
             }
             const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
-            const uint32_t sc = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
-            scc_s[cl * 4 + rb] = static_cast<uint8_t>(sc);
+            scb[half] = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
           }
           if constexpr (FP4) {
-            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, rb, QBC) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(stg + cl * QBW) = make_uint4(out[0], out[1], out[2], out[3]);
           } else {
-            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, 2 * rb, QBC) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-            *reinterpret_cast<uint4*>(qcol_s + cl * QBC + (swz(cl, 2 * rb + 1, QBC) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+            *reinterpret_cast<uint4*>(stg + cl * QBW + (swz(cl, 0, QBW) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(stg + cl * QBW + (swz(cl, 1, QBW) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
           }
         }
-      }
-    }
-
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      if constexpr (DO_ROW) tma_store_2d(&map_qrow, smem_u32(qrow_s), FP4 ? c0 / 2 : c0, r0);
-      if constexpr (DO_COL) tma_store_2d(&map_qcol, smem_u32(qcol_s), FP4 ? r0 / 2 : r0, c0);
-      bulk_commit();
-      if (blockIdx.x + (i + NSTG) * gridDim.x < p.ntiles) { issue(i + NSTG); issued = i + NSTG + 1; }
-    }
-
-    // ------------------------------------------------------------ scales out
-    // One thread per row (row scales) or per column (column scales) writes
-    // that entity's bytes of this tile in the requested layout.
-    if constexpr (!PERTENSOR) {
-      if constexpr (DO_ROW) {
-        if (tid < TR && r0 + tid < p.rows) {
-          const int r = tid, kb = p.cols / 32, b0 = c0 / 32;
-          uint32_t v = 0;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_qcol, smem_u32(stg), FP4 ? (r0 + 32 * rb) / 2 : r0 + 32 * rb, c0);
+          bulk_commit();
+        }
+        // column scales: one byte per column of the lane for this band
+        if constexpr (!PERTENSOR) {
+          const int kb = p.rows / 32, jb = r0 / 32 + rb;
+          if (jb < kb) {
 #pragma unroll
-          for (int b = 0; b < T::ROW_BLOCKS; ++b) v |= static_cast<uint32_t>(scr_s[r * T::ROW_BLOCKS + b]) << (8 * b);
-          uint8_t* dst;
-          bool vec;
-          if (p.sf_mma) {   // full tiles only (rows, cols % 128 == 0)
-            dst = p.s_row + (static_cast<size_t>(r0 / 128) * (p.cols / 128) + c0 / 128) * 512 + (r & 31) * 16 +
-                  ((r >> 5) & 3) * 4 + (c0 & 127) / 32;
-            vec = true;
-          } else {
-            dst = p.s_row + static_cast<size_t>(r0 + r) * kb + b0;
-            vec = (kb % T::ROW_BLOCKS) == 0 && b0 + T::ROW_BLOCKS <= kb;
-          }
-          if (vec) {
-            if constexpr (T::ROW_BLOCKS == 4) *reinterpret_cast<uint32_t*>(dst) = v;
-            else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(v);
-          } else {
-            for (int b = 0; b < T::ROW_BLOCKS && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
-          }
-        }
-      }
-      if constexpr (DO_COL) {
-        if (tid < TC && c0 + tid < p.cols) {
-          const int c = tid, kb = p.rows / 32, b0 = r0 / 32;
-          const uint32_t v = reinterpret_cast<const uint32_t*>(scc_s)[c];
-          if (p.sf_mma) {   // full tiles only
-            const int cc = (c0 & 127) + c;
-            uint8_t* dst = p.s_col + (static_cast<size_t>(c0 / 128) * (p.rows / 128) + r0 / 128) * 512 +
-                           (cc & 31) * 16 + ((cc >> 5) & 3) * 4;
-            *reinterpret_cast<uint32_t*>(dst) = v;
-          } else {
-            uint8_t* dst = p.s_col + static_cast<size_t>(c0 + c) * kb + b0;
-            if ((kb & 3) == 0 && b0 + 4 <= kb) {
-              *reinterpret_cast<uint32_t*>(dst) = v;
-            } else {
-              for (int b = 0; b < 4 && b0 + b < kb; ++b) dst[b] = static_cast<uint8_t>(v >> (8 * b));
+            for (int half = 0; half < 2; ++half) {
+              const int cl = 2 * lane + half;
+              if (c0 + cl < p.cols) {
+                size_t off;
+                if (p.sf_mma) {   // full tiles only
+                  const int cc = (c0 & 127) + cl;
+                  off = (static_cast<size_t>(c0 / 128) * (p.rows / 128) + r0 / 128) * 512 + (cc & 31) * 16 +
+                        ((cc >> 5) & 3) * 4 + rb;
+                } else {
+                  off = static_cast<size_t>(c0 + cl) * kb + jb;
+                }
+                p.s_col[off] = static_cast<uint8_t>(scb[half]);
+              }
             }
           }
         }
       }
+
+      // release the stage; the last of its readers issues its next load
+      if (lane == 0) {
+        const uint32_t old = atomicAdd(&cnt[s], 1u);
+        if (old % ACTIVE == static_cast<uint32_t>(ACTIVE - 1) && blockIdx.x + (i + NSTG) * gridDim.x < p.ntiles)
+          issue(i + NSTG);
+      }
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
-  if (tid == 0) {
-    bulk_wait_all();
-    if (aborted) {
-      for (int j = i; j < issued; ++j) (void)mbar_wait(smem_u32(&bars[j % NSTG]), (j / NSTG) & 1, p.status);
-    }
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    // a wait gave up: let every load still in flight land before the CTA ends
+    for (int st = 0; st < NSTG; ++st)
+      if (last_use[st] >= 0) (void)mbar_wait(smem_u32(&bars[st]), (last_use[st] / NSTG) & 1, p.status);
   }
 
   if constexpr (PERTENSOR) {
@@ -713,20 +713,17 @@ using namespace mxq_host;
 
 namespace {
 
-constexpr int QTC = MXQ_QUANT_TC;
+constexpr int QTC = TileCfg<1, 1, false>::TC;
 constexpr int QNST = MXQ_QUANT_NST;
 constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA>
 int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
                  cudaStream_t st) {
-  using T = TileCfg<QTC, QNST, QSTG, EXTRA>;
-  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QTC, QNST, QSTG>;
-  constexpr bool FP4 = FMT == MXQ_E2M1;
-  constexpr int rowstg = ((TR * (FP4 ? QTC / 2 : QTC)) + 1023) & ~1023;
-  constexpr int colstg = ((QTC * (FP4 ? TR / 2 : TR)) + 1023) & ~1023;
-  // stages, staging tiles, two scale areas, barriers + reduction (256 B), alignment slack
-  constexpr int smem = QNST * T::IN_BYTES + QSTG * (rowstg + colstg) + 512 * 2 + 256 + 1024;
+  using T = TileCfg<QNST, QSTG, EXTRA>;
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG>;
+  // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
+  constexpr int smem = T::SMEM;
   static int per_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -738,7 +735,12 @@ int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap
       return MXQ_ERR_CUDA;
     per_sm[dev & 63] = n;
   }
-  const int grid = std::min(p.ntiles, per_sm[dev & 63] * sm_count());
+  // as many rounds of tiles as the resident CTAs need, spread evenly over
+  // the fewest CTAs that take them in that many rounds: every CTA then works
+  // until the last round (the tail is at most one tile per CTA shorter)
+  const int slots = per_sm[dev & 63] * sm_count();
+  const int rounds = (p.ntiles + slots - 1) / slots;
+  const int grid = (p.ntiles + rounds - 1) / rounds;
   return launch_pdl(kern, dim3(grid), dim3(T::THREADS), smem, st, mx, mr, mc, p);
 }
 
@@ -763,28 +765,33 @@ bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E5M2 || f == MXQ_E2M1; 
 bool valid_orient(int o) { return o == MXQ_ROW || o == MXQ_COL || o == MXQ_DUAL; }
 
 CUtensorMapSwizzle swizzle_for(int pitch) {
-  return pitch >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (pitch == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  return pitch >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                      : (pitch == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                     : (pitch == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE));
 }
 
-// Tensor maps of the tile kernel: input boxes (128 rows x 64 bf16), row
-// codes (128 rows x tile-width bytes), transposed codes (tile-width columns x
-// 128 rows of bytes); the staging swizzle follows the staged row pitch.
+// Tensor maps of the tile kernel: input boxes (128 rows x 64 bf16, 128-byte
+// swizzle); row codes in boxes of one row warp's rows (32 in dual mode, 16
+// row-only) x the tile's code bytes; transposed codes in boxes of the
+// tile's 64 columns x one 32-row band of code bytes.  The staging swizzle
+// follows the staged row pitch.
 int make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, bool fp4, int orient, void* q_row,
               void* q_col, CUtensorMap* mx, CUtensorMap* mr, CUtensorMap* mc) {
-  if (!encode_2d(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, cols, rows, ld * 2, 64, TR, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, cols, rows, ld * 2, QTC, TR, CU_TENSOR_MAP_SWIZZLE_128B))
     return MXQ_ERR_CUDA;
   *mr = *mx;
   *mc = *mx;
   if (orient & MXQ_ROW) {
     const uint64_t inner = fp4 ? cols / 2 : cols;
     const int qbr = fp4 ? QTC / 2 : QTC;
-    if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qbr, TR, swizzle_for(qbr)))
+    const int rr = orient == MXQ_DUAL ? 32 : 16;
+    if (!encode_2d(mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, inner, rows, inner, qbr, rr, swizzle_for(qbr)))
       return MXQ_ERR_CUDA;
   }
   if (orient & MXQ_COL) {
     const uint64_t inner = fp4 ? rows / 2 : rows;
-    const int qbc = fp4 ? TR / 2 : TR;
-    if (!encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, inner, cols, inner, qbc, QTC, swizzle_for(qbc)))
+    const int qbw = fp4 ? 16 : 32;
+    if (!encode_2d(mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, inner, cols, inner, qbw, QTC, swizzle_for(qbw)))
       return MXQ_ERR_CUDA;
   }
   return MXQ_OK;
