@@ -364,6 +364,17 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     fn = lambda: mxq.mm_fp8(x8, w8, X["one"], trans_b=True, bias=X["bias"], fmt="e4m3")
     n += extra_gemm_row(args, fn, timed, "fp8_pertensor_gemm_bias_8192x4096x4096", M, 4096, K, bf16, peak_src,
                         gemm_rows)
+    # a product whose last wave of 256 x 256 tiles is sparse (80 tiles on the
+    # GPU's 76 CTA pairs): the stream-K schedule (default) against the plain one
+    Ms, Ns, Ks = 2560, 2048, 16384
+    xs = q(inputs_tail(X, "a", Ms, Ks), "e4m3", "floor", "row")
+    ws_ = q(inputs_tail(X, "b", Ns, Ks), "e4m3", "floor", "row")
+    fn = lambda: mxq.mx_gemm(xs[0], xs[1], ws_[0], ws_[1], "e4m3")
+    n += extra_gemm_row(args, fn, timed, "mxfp8_sparse_tail_stream_k_2560x2048x16384", Ms, Ns, Ks, bf16, peak_src,
+                        gemm_rows)
+    fn = lambda: mxq.mx_gemm(xs[0], xs[1], ws_[0], ws_[1], "e4m3", stream_k=False)
+    n += extra_gemm_row(args, fn, timed, "mxfp8_sparse_tail_plain_2560x2048x16384", Ms, Ns, Ks, bf16, peak_src,
+                        gemm_rows)
     # the default layout of mm_fp8: b stored row-major [K][N] (the per-tensor
     # quantizer's transposed copy of the [N][K] weight), read N-contiguous
     w8kn = mxq.fp8_quantize_pertensor(W, X["one"], "e4m3", "col")[1]
@@ -371,6 +382,16 @@ def gemm_part(args, mxq, X, q, outs, timed, bf16, peak_src, gemm_rows):
     n += extra_gemm_row(args, fn, timed, "fp8_pertensor_gemm_bias_kn_weight_8192x4096x4096", M, 4096, K, bf16,
                         peak_src, gemm_rows)
     return n
+
+
+def inputs_tail(X, which, rows, K):
+    """Operands of the sparse-tail product: N(0,1) activations with outlier
+    columns (seed 0) and N(0,0.02^2) weights (seed 4), on the device."""
+    from block_scaled_precision_02_gb300 import inputs
+    dev = X["A"].device
+    if which == "a":
+        return inputs.activations(rows, K, seed=0).to(dev)
+    return inputs.weights(rows, K, seed=4).to(dev)
 
 
 def extra_gemm_row(args, fn, timed, name, M, N, K, bf16, peak_src, gemm_rows):

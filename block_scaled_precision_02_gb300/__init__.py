@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
     L.fp8_ring_fold.argtypes = [vp, vp, i32, i32, f32, f32, vp]
     L.mxq_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i32, vp]
     L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
+    L.mxq_gemm_workspace_size.argtypes = [vp]
+    L.mxq_gemm_ws.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp, ctypes.c_size_t, vp]
     L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
@@ -69,7 +71,7 @@ def load() -> ctypes.CDLL:
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
     for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
-                 "mxq_gemm_mixed",
+                 "mxq_gemm_mixed", "mxq_gemm_workspace_size", "mxq_gemm_ws",
                  "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32
@@ -279,19 +281,46 @@ def ring_state_new(hist_len: int = 16, device="cuda") -> torch.Tensor:
 
 
 # --------------------------------------------------------------------------- GEMM
+_WS = {}
+
+
+def gemm_workspace(device: torch.device) -> torch.Tensor:
+    """The stream-K workspace the binding passes to mxq_gemm_ws for torch's
+    current stream on ``device``: allocated (and zero-filled) by torch on
+    first use, then kept; one per stream, because calls that share a
+    workspace must not overlap on the GPU."""
+    device = torch.device(device)
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    w = _WS.get(key)
+    if w is None:
+        n = ctypes.c_size_t(0)
+        with torch.cuda.device(device):
+            _check(load().mxq_gemm_workspace_size(ctypes.byref(n)), "mxq_gemm_workspace_size")
+        w = torch.zeros(n.value, dtype=torch.uint8, device=device)
+        _WS[key] = w
+    return w
+
+
 def mx_gemm(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s: torch.Tensor, fmt="e4m3",
-            out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None, b_fmt=None) -> torch.Tensor:
+            out_dtype=torch.bfloat16, sf_layout="mma", K: Optional[int] = None, b_fmt=None,
+            stream_k: bool = True) -> torch.Tensor:
     """C = A * B^T from MX operands (A [M][K], B [N][K] codes, scales in the
     MMA layout).  ``fmt`` is A's element format and B's unless ``b_fmt`` is
     given (any two of E4M3, E5M2 and E2M1: an E2M1 operand beside an 8-bit
-    one runs at the 8-bit rate).  Returns bf16 (or float32) [M][N]."""
+    one runs at the 8-bit rate).  Returns bf16 (or float32) [M][N].  Runs
+    the stream-K schedule of mxq_gemm_ws with this stream's workspace, unless
+    ``stream_k`` is False (mxq_gemm / mxq_gemm_mixed)."""
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
     if out_dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
     M, N, K = _mx_operands(a_q, a_s, f, b_q, b_s, fb, K)
     c = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
-    if fb == f:
+    if stream_k:
+        ws = gemm_workspace(a_q.device)
+        _call("mxq_gemm_ws", a_q.device, _ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K,
+              _SF[sf_layout], _ptr(c), int(out_dtype == torch.float32), _ptr(ws), ws.numel())
+    elif fb == f:
         _call("mxq_gemm", a_q.device, _ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, f, _SF[sf_layout],
               _ptr(c), int(out_dtype == torch.float32))
     else:

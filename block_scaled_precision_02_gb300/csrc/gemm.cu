@@ -47,6 +47,7 @@
 // MXQ_ERR_TIMEOUT, all roles wind down, in-flight copies are awaited (with a
 // limit) and tensor memory is released.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -100,6 +101,16 @@ struct Params {
   uint32_t a_type, b_type;   // element type codes of the instruction descriptor
   int a_mn, b_mn;     // per-tensor kind: operand stored MN-major ([K][M] / [K][N] rows), else K-major
   int m_fast;         // tile order: M index fastest (A resident in L2), else N fastest
+  // stream-K (CTA-pair kernel, bf16 / float32 output of block-scaled kinds):
+  // tiles [0, sk_dp) go round-robin over the pairs; the k-iterations of the
+  // rest are split into even ranges, one per pair.  A tile cut by a range
+  // boundary b is finished by whichever of its two pieces ends second, which
+  // adds the float32 sums the other parked in workspace slot b.
+  int sk;             // 1: stream-K schedule
+  int sk_dp;          // tiles of the round-robin part
+  float* sk_part;     // per slot and CTA half: 256 columns x 128 rows of float32 (column-major)
+  uint32_t* sk_flags; // per slot and CTA half: ticket word, ready word
+  uint32_t sk_epoch;  // this launch's tag (tickets and ready words never need clearing)
   uint32_t tx_bytes;  // bytes the loads of one stage complete on its "full" barrier (both CTAs of a pair)
   int stall_u;        // failure-detection test hook: CTA 0 never fills this stage use (-1: off)
 };
@@ -117,6 +128,61 @@ __device__ __forceinline__ TilePos tile_pos(const Params& p, int tile, int tm, i
   const int b = tile / per, r = tile - b * per;
   if (p.m_fast) return {b, (r % p.tiles_m) * tm, (r / p.tiles_m) * tn};
   return {b, (r / p.tiles_n) * tm, (r % p.tiles_n) * tn};
+}
+
+// One piece of work of a CTA pair: k-blocks [kb0, kb1) of output tile
+// `tile`.  slot > 0: the tile is cut at range boundary `slot` (the other piece
+// belongs to the neighbouring pair); slot == 0: the whole tile.
+struct Seg {
+  int tile, kb0, kb1, slot;
+};
+
+// The pieces of pair `pair`, in order.  Without stream-K: tiles pair,
+// pair + npairs, ...  With it: those of the round-robin part, then the pair's
+// contiguous range of the remaining k-iterations (iteration = tile *
+// kblocks + k-block).  The host guarantees every range is at least one tile
+// long, so a tile is cut at most once.
+template <bool SK>
+struct SegIter {
+  int tile, step, dp, kblocks, pair;
+  int64_t it, hi;
+  __device__ __forceinline__ SegIter(const Params& p, int pair_, int npairs) {
+    pair = pair_;
+    tile = pair_;
+    step = npairs;
+    kblocks = p.kblocks;
+    dp = SK ? p.sk_dp : p.ntiles;
+    it = hi = 0;
+    if (SK) {
+      const int64_t base = static_cast<int64_t>(p.sk_dp) * p.kblocks;
+      const int64_t rest = static_cast<int64_t>(p.ntiles - p.sk_dp) * p.kblocks;
+      it = base + rest * pair_ / npairs;
+      hi = base + rest * (pair_ + 1) / npairs;
+    }
+  }
+  __device__ __forceinline__ bool next(Seg& sg) {
+    if (tile < dp) {
+      sg = Seg{tile, 0, kblocks, 0};
+      tile += step;
+      return true;
+    }
+    if (!SK || it >= hi) return false;
+    const int t = static_cast<int>(it / kblocks);
+    const int k0 = static_cast<int>(it - static_cast<int64_t>(t) * kblocks);
+    const int k1 = static_cast<int>(min(static_cast<int64_t>(kblocks), k0 + (hi - it)));
+    sg = Seg{t, k0, k1, k0 > 0 ? pair : (k1 < kblocks ? pair + 1 : 0)};
+    it += k1 - k0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05 wrappers
@@ -515,6 +581,104 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
   }
 }
 
+// Stream-K: the second of a cut tile's two pieces to finish writes the tile
+// (bf16 or float32) from RN32(acc + other), `other` the float32 sums the
+// first parked, column-major (column j of this CTA's 128 rows at
+// other[j * 128 + row]).  Chunk by chunk (32 columns), through the same
+// staging buffers and TMA stores as store_tile; the accumulator is released
+// once its last chunk is read.
+template <int BN, typename Release>
+__device__ __forceinline__ void store_tile_added(const Params& p, uint32_t tmem, int q, int lane, bool leader, int& buf,
+                                                 uint8_t* sOut, const CUtensorMap* map_c, int m0, int n0,
+                                                 Release release, const float* other) {
+  const int row = q * 32 + lane;
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  // the other piece's sums arrive 64 columns at a time, the next batch's
+  // loads in flight while the current one is added and stored
+  float nxt[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) nxt[j] = __ldcg(other + j * 128 + row);
+#pragma unroll
+  for (int cb = 0; cb < BN; cb += 64) {
+    float cur[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) cur[j] = nxt[j];
+    if (cb + 64 < BN) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) nxt[j] = __ldcg(other + (cb + 64 + j) * 128 + row);
+    }
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      const int c0 = cb + 32 * hc;
+      uint32_t v[32];
+      tmem_ld32(lane_addr + c0, v);
+      tmem_ld_wait();
+      if (c0 + 32 == BN) {
+        tc_fence_before();
+        __syncwarp();
+        release();
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), cur[32 * hc + j]));
+      const int nbox = p.epi == EPI_BF16 ? 1 : 2;          // staging boxes of 64 bytes per row
+      for (int h = 0; h < nbox; ++h) {
+        if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        named_bar(1, 128);
+        uint8_t* stg = sOut + buf * STG_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int phys = j ^ ((row >> 1) & 3);                   // 64-byte swizzle
+          uint4 w;
+          if (p.epi == EPI_BF16) {
+            uint32_t b[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * k]),
+                                                              __uint_as_float(v[8 * j + 2 * k + 1]));
+              b[k] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            w = make_uint4(b[0], b[1], b[2], b[3]);
+          } else {
+            w = make_uint4(v[h * 16 + 4 * j], v[h * 16 + 4 * j + 1], v[h * 16 + 4 * j + 2], v[h * 16 + 4 * j + 3]);
+          }
+          *reinterpret_cast<uint4*>(stg + row * 64 + phys * 16) = w;
+        }
+        fence_proxy_async_smem();
+        named_bar(1, 128);
+        if (leader) {
+          tma_store_2d(map_c, smem_u32(stg), p.epi == EPI_BF16 ? n0 + c0 : n0 + c0 + h * 16, m0);
+          bulk_commit();
+        }
+        buf ^= 1;
+      }
+    }
+  }
+}
+
+// Stream-K: the first of a cut tile's two pieces to finish parks this
+// CTA's float32 sums (128 rows x BN columns) in its workspace slot, column
+// by column (a warp's 32 rows make one 128-byte store), then releases the
+// accumulator.
+template <int BN, typename Release>
+__device__ __forceinline__ void park_partial(uint32_t tmem, int q, int lane, float* part, Release release) {
+  const int row = q * 32 + lane;
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; c += 2) {
+    uint32_t v[2][32];
+    tmem_ld32(lane_addr + c * 32, v[0]);
+    tmem_ld32(lane_addr + (c + 1) * 32, v[1]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) __stcg(part + ((c + h) * 32 + j) * 128 + row, __uint_as_float(v[h][j]));
+  }
+  tc_fence_before();
+  __syncwarp();
+  release();
+}
+
 template <int KIND_, int BN>
 struct Cfg {
   static constexpr int KIND = KIND_;
@@ -750,7 +914,7 @@ struct PairCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int KIND, int MXOUT>
+template <int KIND, int MXOUT, bool SK = false>
 __global__ void __launch_bounds__(PairCfg<KIND, MXOUT>::THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
@@ -773,6 +937,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(acc_full + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_full + 3) + 1;
   volatile int* epi_fail = reinterpret_cast<volatile int*>(acc_full + 3) + 2;
+  volatile int* sk_first = reinterpret_cast<volatile int*>(acc_full + 3) + 3;   // stream-K ticket outcome
   uint64_t* sf_full = acc_full + 5;                            // rank 0: a slot's scales are in tensor memory
   uint64_t* sf_drain = sf_full + STAGES_P;                     // rank 0
   // accumulator buffer b: full / empty barriers (the second pair exists when NACC == 2)
@@ -821,15 +986,17 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       int u = 0;                                               // stage use counter
-      for (int tile = pair; tile < p.ntiles && !*abort_flag; tile += npairs) {
-        const TilePos tp = tile_pos(p, tile, 256, 256);
+      SegIter<SK> segs(p, pair, npairs);
+      Seg sg;
+      while (!*abort_flag && segs.next(sg)) {
+        const TilePos tp = tile_pos(p, sg.tile, 256, 256);
         const int m0 = tp.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the product
         const int ar = tp.b * (p.a_batched ? p.M : 0) + m0;
         const int n0r = tp.n0 + static_cast<int>(rank) * 128;  // this CTA's half of B
         const int br = tp.b * (p.b_batched ? p.N : 0) + n0r;
         const int ak = tp.b * (p.a_batched ? p.K : 0);           // first K row (MN-major operands)
         const int bk = tp.b * (p.b_batched ? p.K : 0);
-        for (int kb = 0; kb < p.kblocks; ++kb, ++u) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++u) {
           const int s = u % STAGES_P;
           if (!mbar_wait_suspend(smem_u32(&empty[s]), ((u / STAGES_P) & 1) ^ 1, p.status)) { *abort_flag = 1; break; }
           if (rank == 0 && blockIdx.x == 0 && u == p.stall_u) continue;   // test hook: phase never completes
@@ -871,17 +1038,18 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       uint32_t idesc[4];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) idesc[kk] = mma_idesc<KIND>(p, C::BN, 2 * BM, kk);
-      const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
       uint64_t* ready = C::SCALED ? sf_full : full;
       bool ok = true;
       int s = 0, ph = 0;
-      for (int t = 0; t < my_tiles && ok && !*abort_flag; ++t) {
+      SegIter<SK> segs(p, pair, npairs);
+      Seg sg;
+      for (int t = 0; ok && !*abort_flag && segs.next(sg); ++t) {
         const int ab = C::NACC == 2 ? (t & 1) : 0;            // accumulator buffer and its use parity
         const uint32_t aph = C::NACC == 2 ? ((t >> 1) & 1) : (t & 1);
         const uint32_t dacc = tmem + ab * C::BN;
         if (!mbar_wait_suspend(smem_u32(acce(ab)), aph ^ 1, p.status)) { ok = false; break; }
         tc_fence_after();
-        for (int kb = 0; kb < p.kblocks; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait_suspend(smem_u32(&ready[s]), ph, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfa_t = tmem_sf + s * C::SF_COLS_STAGE;
@@ -892,7 +1060,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t sfa = C::FP4 ? sfa_t + 4 * (kk >> 1) : sfa_t;
             const uint32_t sfb = C::FP4 ? sfb_t + 8 * (kk >> 1) : sfb_t;
-            tc_mma_pair<KIND>(dacc, ad + a_step * kk, bd + b_step * kk, idesc[kk], sfa, sfb, (kb | kk) != 0);
+            tc_mma_pair<KIND>(dacc, ad + a_step * kk, bd + b_step * kk, idesc[kk], sfa, sfb,
+                              (kb != sg.kb0) || (kk != 0));
           }
           tc_commit_pair_both(smem_u32(&empty[s]));            // stage free in both CTAs
           if (++s == STAGES_P) { s = 0; ph ^= 1; }
@@ -914,8 +1083,12 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     if (C::SCALED && lane == 0 && rank == 0) {
       const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 0, 128, 0);
       const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 0, 128, 0);
-      const int my_tiles = pair < p.ntiles ? (p.ntiles - 1 - pair) / npairs + 1 : 0;
-      const int total = my_tiles * p.kblocks;
+      int total = 0;                                           // stage uses of this pair
+      {
+        SegIter<SK> segs(p, pair, npairs);
+        Seg sg;
+        while (segs.next(sg)) total += sg.kb1 - sg.kb0;
+      }
       int s = 0, ph = 0;
       for (int u = 0; u < total && !*abort_flag; ++u) {
         if (!mbar_wait_suspend(smem_u32(&full[s]), ph, p.status)) { *abort_flag = 1; break; }
@@ -945,8 +1118,10 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const uint32_t acc_empty1_r0 = cluster_map(smem_u32(acc_empty1), 0);
     const float alpha = (C::KIND == KIND_F8 && p.alpha) ? *p.alpha : 1.0f;
     int t = 0, buf = 0;
-    for (int tile = pair; tile < p.ntiles; tile += npairs, ++t) {
-      const TilePos tp = tile_pos(p, tile, 256, 256);
+    SegIter<SK> segs(p, pair, npairs);
+    Seg sg;
+    for (; segs.next(sg); ++t) {
+      const TilePos tp = tile_pos(p, sg.tile, 256, 256);
       const int m0 = tp.b * p.M + tp.m0 + static_cast<int>(rank) * BM;   // rows of the batched output
       const int ab = C::NACC == 2 ? (t & 1) : 0;
       const uint32_t aph = C::NACC == 2 ? ((t >> 1) & 1) : (t & 1);
@@ -954,14 +1129,45 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       named_bar(1, 128 * C::EPI_GROUPS);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT>(
-          p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * XS_GROUP_BYTES,
-          &map_c, m0, tp.n0 + grp * C::EPI_COLS, [&] {
+      auto release = [&] {
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(acce(ab)));
           else mbar_arrive_remote(ab ? acc_empty1_r0 : acc_empty_r0);
         }
-      });
+      };
+      if constexpr (SK) {
+        if (sg.slot) {
+          // A cut tile: the first of its two pieces to get here parks its
+          // sums; the second adds them and writes the tile.  The ticket is a
+          // swap of this launch's tag into the slot's word, so nothing needs
+          // clearing between launches.
+          uint32_t* flags = p.sk_flags + (static_cast<size_t>(sg.slot) * 2 + rank) * 2;
+          float* part = p.sk_part + (static_cast<size_t>(sg.slot) * 2 + rank) * (C::BN * 128);
+          if (leader) *sk_first = atomicExch(flags, p.sk_epoch) != p.sk_epoch;
+          named_bar(1, 128);
+          if (*sk_first) {
+            park_partial<C::BN>(tmem, q, lane, part, release);
+            __threadfence();
+            named_bar(1, 128);
+            if (leader) st_release_gpu(flags + 1, p.sk_epoch);
+            continue;
+          }
+          // the first piece is running its epilogue: its sums land shortly
+          if (leader) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (ld_acquire_gpu(flags + 1) != p.sk_epoch) {
+              if (globaltimer_ns() - t0 > kWaitLimitNs) { record_timeout(p.status); break; }
+              __nanosleep(256);
+            }
+          }
+          named_bar(1, 128);
+          store_tile_added<C::BN>(p, tmem, q, lane, leader, buf, sOut, &map_c, m0, tp.n0, release, part);
+          continue;
+        }
+      }
+      store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT>(
+          p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * XS_GROUP_BYTES,
+          &map_c, m0, tp.n0 + grp * C::EPI_COLS, release);
     }
     if (leader) bulk_wait_all();
   }
@@ -1006,7 +1212,37 @@ struct GemmArgs {
   uint8_t* cqT;
   uint8_t* csT;
   int mx_fmt, mx_ceil, mx_sf_mma;
+  void* ws;                       // stream-K workspace (or nullptr)
+  size_t ws_bytes;
 };
+
+// Stream-K workspace: per range boundary (slot) and CTA half a ticket word
+// and a ready word, then per slot and half 256 x 128 float32 partial sums.
+// Slots 1 .. pairs - 1 are used; the layout reserves one per pair.
+constexpr size_t kSkSlotFloats = 2 * 256 * 128;
+// The stream-K schedule is used when the tile schedule's last wave keeps at
+// most this share of the pairs busy.  Measured on GB300: a pair's tensor
+// throughput drops when every pair runs (with 76 pairs busy, a pair takes
+// about twice as long per k-block as with 4), so a partial last wave runs
+// faster per pair and costs less than its share of a wave; only a sparse
+// last wave pays for the cut tiles (80 tiles of 8192-deep MXFP8:
+// 99.9 -> 73.7 us; 104 tiles: 100.5 -> 98.3 us).
+constexpr double kSkMaxLastWave = 0.25;
+size_t sk_flag_bytes(int pairs) { return (static_cast<size_t>(pairs) * 16 + 255) & ~size_t(255); }
+size_t sk_workspace_bytes(int pairs) { return sk_flag_bytes(pairs) + static_cast<size_t>(pairs) * kSkSlotFloats * 4; }
+
+// A fresh tag per launch on each device, never 0 (a zero-filled workspace
+// holds no valid ticket).
+uint32_t next_epoch() {
+  static uint32_t epoch[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  uint32_t& e = epoch[dev & 63];
+  if (++e == 0) e = 1;
+  return e;
+}
 
 Params make_params(const GemmArgs& g, int tm, int tn, int64_t kbytes) {
   Params p{};
@@ -1125,7 +1361,7 @@ int launch(const GemmArgs& g, cudaStream_t st) {
 
 // Co-resident clusters of two for the pair kernel (cached per device and
 // kernel); 0 if the device cannot hold one.
-template <int KIND, int MXOUT>
+template <int KIND, int MXOUT, bool SK>
 int max_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, mxq::gemm::Params),
               int smem, int threads) {
   static int cache[64] = {};
@@ -1180,6 +1416,27 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
   Params p = make_params(g, 256, 256, kbytes);
   if (!p.status) return MXQ_ERR_CUDA;
   p.tx_bytes = 2 * (tx_bytes(Cf::A_BYTES, g.a_u4) + tx_bytes(Cf::B_BYTES, g.b_u4) + Cf::SFA_BYTES + Cf::SFB_BYTES);
+  // Stream-K when a workspace is given and the tiles do not fill whole
+  // waves: all but the last full wave run round-robin, the remaining
+  // pairs..2*pairs-1 tiles' k-iterations are split evenly (every range at
+  // least one tile long).
+  if constexpr (MXOUT == 0 && Cf::NACC == 1) {
+    const int last = p.ntiles % pairs;                     // tiles in the last, partial wave
+    const bool worth = p.ntiles > pairs && last > 0 && last <= kSkMaxLastWave * pairs;
+    if (g.ws && worth) {
+      auto kern = mx_gemm_pair_kernel<KIND, MXOUT, true>;
+      const int sk_pairs = max_pairs<KIND, MXOUT, true>(kern, Cf::SMEM, Cf::THREADS);
+      if (sk_pairs == pairs && g.ws_bytes >= sk_workspace_bytes(pairs)) {
+        p.sk = 1;
+        p.sk_dp = (p.ntiles / pairs - 1) * pairs;
+        p.sk_flags = static_cast<uint32_t*>(g.ws);
+        p.sk_part = reinterpret_cast<float*>(static_cast<uint8_t*>(g.ws) + sk_flag_bytes(pairs));
+        p.sk_epoch = next_epoch();
+        return launch_pdl_cluster(kern, dim3(2 * pairs), dim3(Cf::THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb, mc,
+                                  p);
+      }
+    }
+  }
   const int grid = 2 * std::min(p.ntiles, pairs);
   return launch_pdl_cluster(mx_gemm_pair_kernel<KIND, MXOUT>, dim3(grid), dim3(Cf::THREADS), Cf::SMEM, st, 2, ma, mb, msa,
                             msb, mc, p);
@@ -1191,7 +1448,7 @@ template <int KIND, int MXOUT>
 int dispatch_out(const GemmArgs& g, cudaStream_t st) {
   if (g.M % 256 == 0 && g.N % 256 == 0) {
     using Cf = mxq::gemm::PairCfg<KIND, MXOUT>;
-    const int pairs = max_pairs<KIND, MXOUT>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, Cf::SMEM, Cf::THREADS);
+    const int pairs = max_pairs<KIND, MXOUT, false>(mxq::gemm::mx_gemm_pair_kernel<KIND, MXOUT>, Cf::SMEM, Cf::THREADS);
     if (pairs > 0) return launch_pair<KIND, MXOUT>(g, pairs, st);
   }
   // an MN-major B tile is one 128-element swizzle atom wide
@@ -1260,14 +1517,18 @@ int run_mx(const GemmArgs& g, void* stream) {
 }
 
 int gemm_checked(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s, int b_fmt,
-                 int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32, void* stream) {
+                 int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32, void* stream,
+                 void* ws = nullptr, size_t ws_bytes = 0) {
   GemmArgs g;
   const int rc = check_mx(g, a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout);
   if (rc != MXQ_OK) return rc;
   if (!c) return MXQ_ERR_BAD_ARG;
   if (!aligned16(c)) return MXQ_ERR_MISALIGNED;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MXQ_ERR_MISALIGNED;
   g.c = c;
   g.epi = out_fp32 ? mxq::gemm::EPI_FP32 : mxq::gemm::EPI_BF16;
+  g.ws = ws;
+  g.ws_bytes = ws ? ws_bytes : 0;
   return run_mx(g, stream);
 }
 
@@ -1282,6 +1543,20 @@ extern "C" int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt, co
                               int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32,
                               void* stream) {
   return gemm_checked(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout, c, out_fp32, stream);
+}
+
+extern "C" int mxq_gemm_workspace_size(size_t* bytes) {
+  if (!bytes) return MXQ_ERR_BAD_ARG;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  *bytes = sk_workspace_bytes(sm_count() / 2);
+  return MXQ_OK;
+}
+
+extern "C" int mxq_gemm_ws(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
+                           int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_checked(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout, c, out_fp32, stream, workspace,
+                      workspace_bytes);
 }
 
 extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,

@@ -207,6 +207,31 @@ int mxq_gemm_mixed(const void* a_q, const uint8_t* a_s, int a_fmt,
                    int64_t M, int64_t N, int64_t K, int sf_layout, void* c,
                    int out_fp32, void* stream);
 
+/* ---- block-scaled GEMM with a stream-K schedule ----------------------------
+ * The product of mxq_gemm_mixed (same arguments, same output).  With a
+ * workspace the CTA-pair kernel (M and N multiples of 256, bf16 or float32
+ * output) balances its last waves: when the last wave of 256 x 256 output
+ * tiles would keep at most a quarter of the GPU's CTA pairs busy, the
+ * k-iterations of the last one to two waves of tiles are split into even
+ * contiguous ranges, one per pair, and a tile cut by a
+ * range boundary is finished by whichever of its two pieces ends second,
+ * which adds the float32 sums the other parked in the workspace (so such a
+ * tile's sum is RN32(first piece + second piece), a rounding order that
+ * differs from an uncut tile within the float32 accumulation error; the
+ * result does not depend on which piece ends first).
+ * workspace  device memory of at least mxq_gemm_workspace_size bytes,
+ *            256-byte aligned, zero-filled before its first use (the library
+ *            keeps it valid afterwards).  Calls that share a workspace must
+ *            not run concurrently (order them on one stream).  NULL, or
+ *            fewer bytes, runs mxq_gemm_mixed's schedule.
+ * Shapes and alignment as mxq_gemm_mixed. */
+int mxq_gemm_workspace_size(size_t* bytes);
+int mxq_gemm_ws(const void* a_q, const uint8_t* a_s, int a_fmt,
+                const void* b_q, const uint8_t* b_s, int b_fmt,
+                int64_t M, int64_t N, int64_t K, int sf_layout, void* c,
+                int out_fp32, void* workspace, size_t workspace_bytes,
+                void* stream);
+
 /* ---- block-scaled GEMM with an MX output (FAF article: producers emit the
  * format and scale layout their consumer reads, with no bf16 round trip;
  * gap section 2: row-wise and column-wise copies) -----------------------------

@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
-              "mxq_gemm_mixed",
+              "mxq_gemm_mixed", "mxq_gemm_ws", "mxq_gemm_workspace_size",
               "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
               "mxq_last_device_status", "mxq_strerror", "mxq_version"):
         assert n in names
@@ -128,6 +128,11 @@ def test_argument_checks_need_no_gpu(so):
     assert mm(FAKE, FAKE, 0, 128, 128, 128, 0, 0, 0, 1, 0, FAKE, None, FAKE, None) == -2   # batch 0
     assert mm(FAKE, FAKE, 1, 100, 128, 128, 0, 0, 1, 0, 0, FAKE, None, FAKE, None) == -2
     assert mm(FAKE, FAKE, 1, 128, 128, 128, 0, 0, 0, 0, 0, FAKE, ODD, FAKE, None) == -3   # bias alignment
+
+    assert so.mxq_gemm_workspace_size(None) == -1
+    ws = so.mxq_gemm_ws
+    assert ws(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 256, 128, 1, FAKE, 0, ODD, 1 << 20, None) == -3   # workspace alignment
+    assert ws(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 100, 128, 1, FAKE, 0, FAKE, 1 << 20, None) == -2
 
     rf = so.fp8_ring_fold
     assert rf(None, FAKE, 16, 0, 448.0, 1.0, None) == -1           # no amax

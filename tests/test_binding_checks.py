@@ -77,7 +77,9 @@ def test_every_library_call_runs_with_the_tensors_device_current(monkeypatch):
     tree = ast.parse(src)
     direct = []
     for fn in ast.walk(tree):
-        if isinstance(fn, ast.FunctionDef) and fn.name not in ("_call", "load", "lib", "last_device_status"):
+        # these guard the device themselves (with torch.cuda.device)
+        if isinstance(fn, ast.FunctionDef) and fn.name not in ("_call", "load", "lib", "last_device_status",
+                                                               "gemm_workspace"):
             for node in ast.walk(fn):
                 if (isinstance(node, ast.Call) and isinstance(node.func, ast.Attribute)
                         and isinstance(node.func.value, ast.Call) and getattr(node.func.value.func, "id", "") == "load"):
