@@ -62,6 +62,7 @@ def load() -> ctypes.CDLL:
     L.mxq_gemm_mixed.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
     L.mxq_gemm_workspace_size.argtypes = [vp]
     L.mxq_gemm_ws.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp, ctypes.c_size_t, vp]
+    L.mxq_gemm_noalloc.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, i32, vp]
     L.mxq_gemm_mx_out.argtypes = [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.mxq_mm_fp8.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     L.mxq_sf_to_mma.argtypes = [vp, i64, i64, vp, vp]
@@ -71,7 +72,7 @@ def load() -> ctypes.CDLL:
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
     for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
-                 "mxq_gemm_mixed", "mxq_gemm_workspace_size", "mxq_gemm_ws",
+                 "mxq_gemm_mixed", "mxq_gemm_workspace_size", "mxq_gemm_ws", "mxq_gemm_noalloc",
                  "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
         getattr(L, name).restype = i32

@@ -1559,6 +1559,50 @@ extern "C" int mxq_gemm_ws(const void* a_q, const uint8_t* a_s, int a_fmt, const
                       workspace_bytes);
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch of mxq_gemm_noalloc: the stream-K workspace of mxq_gemm_ws, held
+// in the library itself for callers that cannot allocate device memory.
+// Every device that loads the library holds this array until the process
+// exits.  It covers up to 80 CTA pairs (160 SMs).
+constexpr size_t kNoAllocScratchBytes = MXQ_GEMM_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes >= 80 * kSkSlotFloats * 4 + 80 * 16 + 256, "scratch covers 80 pairs");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (in host code the array's name is not a device address).
+int noalloc_scratch(void** out) {
+  static void* ptr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MXQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MXQ_ERR_CUDA;
+    ptr[dev] = p;
+  }
+  *out = ptr[dev];
+  return MXQ_OK;
+}
+
+extern "C" int mxq_gemm_noalloc(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
+                                int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, void* c, int out_fp32,
+                                void* stream) {
+  GemmArgs g;
+  const int rc = check_mx(g, a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout);
+  if (rc != MXQ_OK) return rc;
+  if (!c) return MXQ_ERR_BAD_ARG;
+  if (!aligned16(c)) return MXQ_ERR_MISALIGNED;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  // the scratch this device's stream-K schedule can need, against the array
+  if (sk_workspace_bytes(sm_count() / 2) > kNoAllocScratchBytes) return MXQ_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  const int src = noalloc_scratch(&ws);
+  if (src != MXQ_OK) return src;
+  return gemm_checked(a_q, a_s, a_fmt, b_q, b_s, b_fmt, M, N, K, sf_layout, c, out_fp32, stream, ws,
+                      kNoAllocScratchBytes);
+}
+
 extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, const void* b_q, const uint8_t* b_s,
                                int b_fmt, int64_t M, int64_t N, int64_t K, int sf_layout, int out_fmt,
                                int out_scale_mode, int out_sf_layout, uint8_t* c_q, uint8_t* c_s, uint8_t* c_qT,

@@ -232,6 +232,35 @@ int mxq_gemm_ws(const void* a_q, const uint8_t* a_s, int a_fmt,
                 int out_fp32, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/* ---- mxq_gemm_ws without a caller workspace (no counterpart on the pages:
+ * an entry point of this library for callers that cannot allocate) -----------
+ * Some callers cannot allocate device memory when they call: code running
+ * inside another framework's executor that owns all of the device's memory,
+ * or a plugin whose execute step is not allowed to allocate.  This call runs
+ * the product of mxq_gemm_ws with the library's own scratch instead of a
+ * caller workspace: a static array of MXQ_GEMM_NOALLOC_SCRATCH_BYTES in
+ * device memory, which every device that loads the library holds until the
+ * process exits.  The call itself allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array, which keeps what the last
+ *    call left there.  Its ticket words carry a tag that is new for every
+ *    launch, so nothing in it has to start at zero for a call (the array is
+ *    zero when the library loads).  Calls that overlap on the GPU (on
+ *    different streams, or from different threads without ordering) race
+ *    on the array: order them on one stream.
+ *  - The array covers the stream-K scratch of up to 80 CTA pairs (a GPU of
+ *    up to 160 SMs); on a device that would need more the call returns
+ *    MXQ_ERR_UNSUPPORTED and launches nothing.
+ * Arguments, shapes, alignment and output as mxq_gemm_ws. */
+#define MXQ_GEMM_NOALLOC_SCRATCH_BYTES ((size_t)20 * 1024 * 1024 + 4096)
+int mxq_gemm_noalloc(const void* a_q, const uint8_t* a_s, int a_fmt,
+                     const void* b_q, const uint8_t* b_s, int b_fmt,
+                     int64_t M, int64_t N, int64_t K, int sf_layout,
+                     void* c, int out_fp32, void* stream);
+
 /* ---- block-scaled GEMM with an MX output (FAF article: producers emit the
  * format and scale layout their consumer reads, with no bf16 round trip;
  * gap section 2: row-wise and column-wise copies) -----------------------------
