@@ -463,6 +463,60 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     }
     return;
   }
+  if constexpr (MXOUT != 0 && BN <= 128) {
+    // At most 128 columns per thread (the pair kernel's two epilogue
+    // groups): read all of them into registers and release the accumulator
+    // first, so the MMAs of the next tile run while this one is quantized.
+    uint32_t v[BN / 32][32];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + c * 32, v[c]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    release();
+    uint32_t sc[BN / 128 > 0 ? BN / 128 : 1];
+#pragma unroll
+    for (int g = 0; g < (BN / 128 > 0 ? BN / 128 : 1); ++g) sc[g] = 0;
+    uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * XS_WORDS;    // this warp's transpose scratch
+    const size_t rg = static_cast<size_t>(m0 + row);
+    const size_t rT = static_cast<size_t>(m0 + q * 32);          // first row of the warp's column blocks
+    const bool rows_out = MXOUT == 1 || p.cq, cols_out = MXOUT == 2 && p.cqT;
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      if (rows_out) {
+        uint32_t cr[8];
+        const uint32_t s8 = mx_block32(v[c], p.mx_fmt, p.mx_ceil, cr);
+        sc[c >> 2] |= s8 << (8 * (c & 3));
+        uint4* d = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0 + c * 32);
+        d[0] = make_uint4(cr[0], cr[1], cr[2], cr[3]);
+        d[1] = make_uint4(cr[4], cr[5], cr[6], cr[7]);
+      }
+      if (cols_out) {
+        // a warp's 32 rows of the chunk are 32 column blocks: transposed
+        // through the warp's scratch, lane j takes column j
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(xs + lane * XS_PITCH + 4 * j) =
+              make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3]);
+        __syncwarp();
+        uint32_t col[32], cc[8];
+        load_col32(xs, lane, col);
+        __syncwarp();
+        const uint32_t sT = mx_block32(col, p.mx_fmt, p.mx_ceil, cc);
+        const size_t n = static_cast<size_t>(n0 + c * 32 + lane);
+        uint4* dT = reinterpret_cast<uint4*>(p.cqT + n * static_cast<size_t>(p.M) + rT);
+        dT[0] = make_uint4(cc[0], cc[1], cc[2], cc[3]);
+        dT[1] = make_uint4(cc[4], cc[5], cc[6], cc[7]);
+        const size_t kbT = static_cast<size_t>(p.M / 32), jT = rT / 32;
+        const size_t offT = p.mx_sf_mma
+                                ? ((n / 128) * (kbT / 4) + jT / 4) * 512 + (n % 32) * 16 + ((n / 32) % 4) * 4 + jT % 4
+                                : n * kbT + jT;
+        p.csT[offT] = static_cast<uint8_t>(sT);
+      }
+    }
+    if (rows_out) store_row_scales<BN>(p, rg, n0, sc);
+    return;
+  }
   if constexpr (MXOUT == 1) {
     // row blocks only: each 32-column chunk of a row is one MX block; codes
     // and scale bytes are formed in registers, the accumulator is released,
