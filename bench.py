@@ -705,23 +705,31 @@ def run_ours(args, rank, world):
     # ---------------- e2e through the public API: host buffers, copies inside
     A_pin, G_pin = A_h.pin_memory(), G_h.pin_memory()
     out_pin = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o) for o in outs]
-    A_d, G_d = torch.empty_like(A), torch.empty_like(G)
+    # two device copies of the inputs, used by alternate steps, so the next
+    # step's input copy overlaps this step's kernels
+    A_d = [torch.empty_like(A) for _ in range(2)]
+    G_d = [torch.empty_like(G) for _ in range(2)]
 
     # Three streams: inputs in, quantize, results out.  The host link is
     # full duplex, so the next input copy, the kernels and the previous
     # result copies overlap; every byte still crosses inside the timed loop.
     s_cmp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    kernels_done = [None, None]                 # per input set: the last step's kernels on it
+    step_no = {"k": 0}
 
     def e2e_step():
-        s_in.wait_stream(s_cmp)                 # the previous step's kernels are done with A_d / G_d
+        b = step_no["k"] % 2
+        step_no["k"] += 1
+        if kernels_done[b] is not None:
+            s_in.wait_event(kernels_done[b])    # the step before last is done with this input set
         with torch.cuda.stream(s_in):
-            A_d.copy_(A_pin, non_blocking=True)
+            A_d[b].copy_(A_pin, non_blocking=True)
             ev_a = s_in.record_event()
-            G_d.copy_(G_pin, non_blocking=True)
+            G_d[b].copy_(G_pin, non_blocking=True)
             ev_g = s_in.record_event()
-        for i, (x, fmt, mode) in enumerate(((A_d, "e4m3", "floor"), (A_d, "e4m3", "ceil"),
-                                             (G_d, "e5m2", "floor"), (G_d, "e5m2", "ceil"))):
+        for i, (x, fmt, mode) in enumerate(((A_d[b], "e4m3", "floor"), (A_d[b], "e4m3", "ceil"),
+                                             (G_d[b], "e5m2", "floor"), (G_d[b], "e5m2", "ceil"))):
             s_cmp.wait_event(ev_a if i < 2 else ev_g)
             res = q(x, fmt, mode)
             done = s_cmp.record_event()
@@ -730,6 +738,7 @@ def run_ours(args, rank, world):
                 for h, d in zip(out_pin[i], res):
                     d.record_stream(s_out)      # not reused before its copy has finished
                     h.copy_(d, non_blocking=True)
+        kernels_done[b] = s_cmp.record_event()
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
@@ -767,7 +776,8 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(step_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3),
                 "api": "block_scaled_precision_02_gb300.mx_quantize (pinned host in, pinned host out)",
-                "streams": "inputs in, quantize and results out on three streams (copies overlap the kernels and each other)"},
+                "streams": ("inputs in, quantize and results out on three streams (copies overlap the kernels and "
+                            "each other); two device input buffers used by alternate steps")},
         "gpu_launches": launches,
         "gpu_launches_detail": launch_detail,
         "gemm": {"metric": "MX GEMM TFLOP/s", "rows": gemm_rows, "cpu_baseline": gcpu},
