@@ -1,5 +1,6 @@
-// GEMMs on the sm_103a tensor cores, C = A * B^T with both operands
-// K-contiguous and float32 accumulation in tensor memory:
+// GEMMs on the sm_103a tensor cores, C = A * B^T with float32 accumulation
+// in tensor memory (block-scaled operands K-contiguous; per-tensor FP8
+// operands K-contiguous or M / N-contiguous):
 //  * block-scaled (MX):
 //      C[m][n] = sum_k dec(a[m][k]) 2^(sa[m][k/32]-127) dec(b[n][k]) 2^(sb[n][k/32]-127)
 //    Source: "UE8M0 FP8 / MXFP8 explainer", section 1 -- tensor cores consume
@@ -9,7 +10,8 @@
 //    (format-aware fusion: the producer writes its consumer's format) MX
 //    codes and scales of 1 x 32 row blocks quantized from the accumulator.
 //  * per-tensor FP8 (AstrAI fp8.py, mm_fp8): C = (A * B^T) * scale + bias,
-//    bf16 out, optionally batched.
+//    bf16 out, optionally batched; an operand stored [K][M] / [K][N] is read
+//    in place through MN-major tiles.
 //
 // Two kernels share the warp roles below.
 //  * CTA pair (M and N multiples of 256): clusters of two CTAs on two SMs
@@ -19,6 +21,10 @@
 //    per K step instead of 48 KB.  Scale chunks: each CTA holds its own rows
 //    of A's scales and all 256 rows of B's; one tcgen05.cp.cta_group::2
 //    fills both CTAs' tensor memory from the same offset.
+//    Tiles run in waves of consecutive indices, ordered so the smaller
+//    operand stays in L2.  A stream-K variant (a separate instantiation)
+//    evens out a sparse last wave by splitting k-ranges over the pairs; cut
+//    tiles meet through a caller workspace or the library's static scratch.
 //  * single CTA (otherwise): 128 x BN tiles, tcgen05.mma.cta_group::1.
 // Roles (one CTA per SM, persistent over output tiles):
 //  * warp 0      TMA producer: per K step (128 bytes of codes per row) the
@@ -38,7 +44,9 @@
 //                and stores (TMA through two 64-byte-swizzled staging
 //                buffers; the MX output is stored directly).  The pair
 //                kernel's MX-output variants add warps 7..10, a second
-//                epilogue group that takes the other half of the columns.
+//                epilogue group that takes the other half of the columns,
+//                and read all of a group's columns into registers before
+//                releasing the accumulator.
 // Operands: E4M3 / E5M2 / E2M1 in any pairing.  Packed E2M1 beside an 8-bit
 // operand is widened to one byte per code by its tensor map on the way into
 // shared memory (the 4-bit layout of kind::mxf8f6f4), so both operands then
