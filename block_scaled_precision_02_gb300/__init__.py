@@ -337,19 +337,21 @@ def mx_gemm_mx_out(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor, b_s:
     accumulator: row blocks (1x32 along N) and/or column blocks (32x1 along
     M, stored transposed), per ``orientation`` ("row", "col", "dual").
     Returns (codes [M][N], scales [M][N/32], codesT [N][M], scalesT [N][M/32])
-    with None for an orientation not requested; MMA-layout scales hold the
+    with None for an orientation not requested (``out_fmt`` "e2m1": codes
+    packed two per byte, [M][N/2] and [N][M/2]); MMA-layout scales hold the
     same number of bytes."""
     f = _FMT[fmt]
     fb = f if b_fmt is None else _FMT[b_fmt]
     o = _ORIENT[orientation]
     M, N, K = _mx_operands(a_q, a_s, f, b_q, b_s, fb, K)
     dev = a_q.device
+    ob = 2 if _FMT[out_fmt] == E2M1 else 1          # E2M1 codes: two per byte
     cq = cs = cqT = csT = None
     if o & ROW:
-        cq = torch.empty(M, N, dtype=torch.uint8, device=dev)
+        cq = torch.empty(M, N // ob, dtype=torch.uint8, device=dev)
         cs = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
     if o & COL:
-        cqT = torch.empty(N, M, dtype=torch.uint8, device=dev)
+        cqT = torch.empty(N, M // ob, dtype=torch.uint8, device=dev)
         csT = torch.empty(N, M // 32, dtype=torch.uint8, device=dev)
     _call("mxq_gemm_mx_out", dev, _ptr(a_q), _ptr(a_s), f, _ptr(b_q), _ptr(b_s), fb, M, N, K, SF_MMA,
           _FMT[out_fmt], _SCALE[out_scale_mode], _SF[out_sf_layout], _ptr(cq), _ptr(cs), _ptr(cqT), _ptr(csT))

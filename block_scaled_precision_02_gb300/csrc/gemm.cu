@@ -381,6 +381,46 @@ __device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt,
   return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
 }
 
+// The same for E2M1 output: codes in 4 words, eight nibbles each (element 0
+// in the lowest nibble).
+__device__ __forceinline__ uint32_t mx_block32_e2m1(const uint32_t (&v)[32], int ceil_mode, uint32_t* codes /* 4 words */) {
+  uint32_t ab = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ab = max(ab, v[j] & 0x7FFFFFFFu);
+  const bool bad = ab >= 0x7F800000u;
+  const int e = bad ? 0 : scale_exp<MXQ_E2M1>(ab, ceil_mode);
+  const float m = exp2_neg(e);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x |= cvt_e2m1x2(__fmul_rn(__uint_as_float(v[8 * k + 2 * j]), m), __fmul_rn(__uint_as_float(v[8 * k + 2 * j + 1]), m))
+           << (8 * j);
+    codes[k] = bad ? 0u : x;
+  }
+  return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+}
+
+// One MX block of the output format (FP4O: E2M1, else p.mx_fmt), codes
+// stored at dst (32 bytes of FP8 or 16 of packed E2M1); returns the scale.
+template <bool FP4O>
+__device__ __forceinline__ uint32_t mx_block_store(const uint32_t (&v)[32], const Params& p, uint8_t* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  if constexpr (FP4O) {
+    uint32_t c[4];
+    const uint32_t s = mx_block32_e2m1(v, p.mx_ceil, c);
+    d[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    return s;
+  } else {
+    uint32_t c[8];
+    const uint32_t s = mx_block32(v, p.mx_fmt, p.mx_ceil, c);
+    d[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    d[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    return s;
+  }
+}
+
 // Column `lane` of the warp's chunk, read once from the transpose scratch.
 __device__ __forceinline__ void load_col32(const uint32_t* xs, int lane, uint32_t (&v)[32]) {
 #pragma unroll
@@ -415,6 +455,10 @@ template <int BN, bool PER_TENSOR, int MXOUT, typename Release>
 __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_t tmem, int q, int lane, bool leader,
                                            int& buf, uint8_t* sOut, const CUtensorMap* map_c, int m0, int n0,
                                            Release release) {
+  // MX outputs: 1 rows, 2 rows + columns (FP8 codes); 3, 4 the same in E2M1
+  constexpr int ORI = MXOUT > 2 ? MXOUT - 2 : MXOUT;
+  constexpr bool FP4O = MXOUT > 2;
+  constexpr int CSH = FP4O ? 1 : 0;                        // E2M1: half a byte per code
   const int row = q * 32 + lane;
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
   if (MXOUT == 0 && p.epi == EPI_BF16) {
@@ -488,16 +532,13 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * XS_WORDS;    // this warp's transpose scratch
     const size_t rg = static_cast<size_t>(m0 + row);
     const size_t rT = static_cast<size_t>(m0 + q * 32);          // first row of the warp's column blocks
-    const bool rows_out = MXOUT == 1 || p.cq, cols_out = MXOUT == 2 && p.cqT;
+    const bool rows_out = ORI == 1 || p.cq, cols_out = ORI == 2 && p.cqT;
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       if (rows_out) {
-        uint32_t cr[8];
-        const uint32_t s8 = mx_block32(v[c], p.mx_fmt, p.mx_ceil, cr);
+        const uint32_t s8 =
+            mx_block_store<FP4O>(v[c], p, p.cq + ((rg * static_cast<size_t>(p.N) + n0 + c * 32) >> CSH));
         sc[c >> 2] |= s8 << (8 * (c & 3));
-        uint4* d = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0 + c * 32);
-        d[0] = make_uint4(cr[0], cr[1], cr[2], cr[3]);
-        d[1] = make_uint4(cr[4], cr[5], cr[6], cr[7]);
       }
       if (cols_out) {
         // a warp's 32 rows of the chunk are 32 column blocks: transposed
@@ -507,14 +548,11 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
           *reinterpret_cast<uint4*>(xs + lane * XS_PITCH + 4 * j) =
               make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3]);
         __syncwarp();
-        uint32_t col[32], cc[8];
+        uint32_t col[32];
         load_col32(xs, lane, col);
         __syncwarp();
-        const uint32_t sT = mx_block32(col, p.mx_fmt, p.mx_ceil, cc);
         const size_t n = static_cast<size_t>(n0 + c * 32 + lane);
-        uint4* dT = reinterpret_cast<uint4*>(p.cqT + n * static_cast<size_t>(p.M) + rT);
-        dT[0] = make_uint4(cc[0], cc[1], cc[2], cc[3]);
-        dT[1] = make_uint4(cc[4], cc[5], cc[6], cc[7]);
+        const uint32_t sT = mx_block_store<FP4O>(col, p, p.cqT + ((n * static_cast<size_t>(p.M) + rT) >> CSH));
         const size_t kbT = static_cast<size_t>(p.M / 32), jT = rT / 32;
         const size_t offT = p.mx_sf_mma
                                 ? ((n / 128) * (kbT / 4) + jT / 4) * 512 + (n % 32) * 16 + ((n / 32) % 4) * 4 + jT % 4
@@ -525,12 +563,11 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     if (rows_out) store_row_scales<BN>(p, rg, n0, sc);
     return;
   }
-  if constexpr (MXOUT == 1) {
-    // row blocks only: each 32-column chunk of a row is one MX block; codes
-    // and scale bytes are formed in registers, the accumulator is released,
-    // and then they are stored
-    uint32_t codes[BN / 4];
+  if constexpr (ORI == 1) {
+    // row blocks only: each 32-column chunk of a row is one MX block, formed
+    // and stored chunk by chunk; the accumulator is released at the end
     uint32_t sc[BN / 128];
+    const size_t rg = static_cast<size_t>(m0 + row);
 #pragma unroll
     for (int g = 0; g < BN / 128; ++g) sc[g] = 0;
 #pragma unroll
@@ -541,21 +578,18 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
       tmem_ld_wait();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t s8 = mx_block32(v[h], p.mx_fmt, p.mx_ceil, &codes[(c + h) * 8]);
+        const uint32_t s8 =
+            mx_block_store<FP4O>(v[h], p, p.cq + ((rg * static_cast<size_t>(p.N) + n0 + (c + h) * 32) >> CSH));
         sc[(c + h) >> 2] |= s8 << (8 * ((c + h) & 3));
       }
     }
     tc_fence_before();
     __syncwarp();
     release();
-    const size_t rg = static_cast<size_t>(m0 + row);
-    uint4* dst = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0);
-#pragma unroll
-    for (int i = 0; i < BN / 16; ++i) dst[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
     store_row_scales<BN>(p, rg, n0, sc);
     return;
   }
-  if constexpr (MXOUT == 2) {
+  if constexpr (ORI == 2) {
     // row blocks: each 32-column chunk of a row is one MX block, formed
     // from the registers and stored at once (only the scale words are kept
     // to the end).  Column blocks: a warp's 32 rows of a chunk are 32 blocks
@@ -577,12 +611,9 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (p.cq) {
-          uint32_t cr[8];
-          const uint32_t s8 = mx_block32(v[h], p.mx_fmt, p.mx_ceil, cr);
+          const uint32_t s8 =
+              mx_block_store<FP4O>(v[h], p, p.cq + ((rg * static_cast<size_t>(p.N) + n0 + (c + h) * 32) >> CSH));
           sc[(c + h) >> 2] |= s8 << (8 * ((c + h) & 3));
-          uint4* d = reinterpret_cast<uint4*>(p.cq + rg * static_cast<size_t>(p.N) + n0 + (c + h) * 32);
-          d[0] = make_uint4(cr[0], cr[1], cr[2], cr[3]);
-          d[1] = make_uint4(cr[4], cr[5], cr[6], cr[7]);
         }
         if (p.cqT) {
 #pragma unroll
@@ -590,14 +621,12 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
             *reinterpret_cast<uint4*>(xs + lane * XS_PITCH + 4 * j) =
                 make_uint4(v[h][4 * j], v[h][4 * j + 1], v[h][4 * j + 2], v[h][4 * j + 3]);
           __syncwarp();
-          uint32_t col[32], cc[8];
+          uint32_t col[32];
           load_col32(xs, lane, col);
           __syncwarp();
-          const uint32_t sT = mx_block32(col, p.mx_fmt, p.mx_ceil, cc);
           const size_t n = static_cast<size_t>(n0 + (c + h) * 32 + lane);
-          uint4* dT = reinterpret_cast<uint4*>(p.cqT + n * static_cast<size_t>(p.M) + rT);
-          dT[0] = make_uint4(cc[0], cc[1], cc[2], cc[3]);
-          dT[1] = make_uint4(cc[4], cc[5], cc[6], cc[7]);
+          const uint32_t sT =
+              mx_block_store<FP4O>(col, p, p.cqT + ((n * static_cast<size_t>(p.M) + rT) >> CSH));
           const size_t kbT = static_cast<size_t>(p.M / 32), jT = rT / 32;
           const size_t offT = p.mx_sf_mma
                                   ? ((n / 128) * (kbT / 4) + jT / 4) * 512 + (n % 32) * 16 + ((n / 32) % 4) * 4 + jT % 4
@@ -956,8 +985,9 @@ struct PairCfg {
   static constexpr int EPI_COLS = BN / EPI_GROUPS;      // accumulator columns per epilogue group
   static constexpr int THREADS = PAIR_THREADS + (EPI_GROUPS - 1) * 128;
   // the column-block output transposes through 32 x 33 words per epilogue warp
-  static constexpr int OUT = MXOUT_ == 2 ? EPI_GROUPS * XS_GROUP_BYTES : OUT_BYTES;
-  static constexpr int STAGES = (FP4 || MXOUT_ == 2) ? 5 : 6;
+  static constexpr bool MX_COLS = MXOUT_ == 2 || MXOUT_ == 4;     // MX column blocks too
+  static constexpr int OUT = MX_COLS ? EPI_GROUPS * XS_GROUP_BYTES : OUT_BYTES;
+  static constexpr int STAGES = (FP4 || MX_COLS) ? 5 : 6;
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
   static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
@@ -1525,6 +1555,7 @@ int dispatch(const GemmArgs& g, cudaStream_t st) {
   if constexpr (KIND == mxq::gemm::KIND_F8) return dispatch_out<KIND, 0>(g, st);
   else {
     if (g.epi != mxq::gemm::EPI_MX) return dispatch_out<KIND, 0>(g, st);
+    if (g.mx_fmt == MXQ_E2M1) return g.cqT ? dispatch_out<KIND, 4>(g, st) : dispatch_out<KIND, 3>(g, st);
     return g.cqT ? dispatch_out<KIND, 2>(g, st) : dispatch_out<KIND, 1>(g, st);
   }
 }
@@ -1675,7 +1706,7 @@ extern "C" int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt, c
   if (!c_q != !c_s || !c_qT != !c_sT || (!c_q && !c_qT)) return MXQ_ERR_BAD_ARG;
   if ((c_q && (!aligned16(c_q) || !aligned16(c_s))) || (c_qT && (!aligned16(c_qT) || !aligned16(c_sT))))
     return MXQ_ERR_MISALIGNED;
-  if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2) return out_fmt == MXQ_E2M1 ? MXQ_ERR_UNSUPPORTED : MXQ_ERR_BAD_ARG;
+  if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2 && out_fmt != MXQ_E2M1) return MXQ_ERR_BAD_ARG;
   if (out_scale_mode != MXQ_SCALE_FLOOR_OCP && out_scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
   if (out_sf_layout != MXQ_SF_CANONICAL && out_sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
   g.epi = mxq::gemm::EPI_MX;

@@ -265,18 +265,20 @@ int mxq_gemm_noalloc(const void* a_q, const uint8_t* a_s, int a_fmt,
  * format and scale layout their consumer reads, with no bf16 round trip;
  * gap section 2: row-wise and column-wise copies) -----------------------------
  * Same product as mxq_gemm_mixed.  Instead of C, writes MX codes of out_fmt
- * (MXQ_E4M3 | MXQ_E5M2) with their UE8M0 scales:
- *   c_q, c_s    row blocks (1x32 along each row of C): codes [M][N], scales
- *               canonical [M][N/32] or MXQ_SF_MMA (the layout mxq_gemm reads
- *               for an A operand);
+ * (MXQ_E4M3 | MXQ_E5M2 | MXQ_E2M1) with their UE8M0 scales:
+ *   c_q, c_s    row blocks (1x32 along each row of C): codes [M][N] (E2M1
+ *               packed [M][N/2]), scales canonical [M][N/32] or MXQ_SF_MMA
+ *               (the layout mxq_gemm reads for an A operand);
  *   c_qT, c_sT  column blocks (32x1 along each column of C), stored
- *               transposed: codes [N][M] of C^T, scales canonical [N][M/32]
- *               or MXQ_SF_MMA (the layout of a B operand along M).
+ *               transposed: codes [N][M] of C^T (E2M1 [N][M/2]), scales
+ *               canonical [N][M/32] or MXQ_SF_MMA (the layout of a B operand
+ *               along M).
  * Either pair may be NULL (both of a pair, not one), not both pairs.
  * The block scale (out_scale_mode MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL) and
  * the RNE-saturating element rounding follow mxq_quantize, applied to the
  * float32 accumulator.  A block holding NaN/Inf gets scale 0xFF and zero
- * codes.  Outputs 16-byte aligned.  E2M1 output: MXQ_ERR_UNSUPPORTED. */
+ * codes.  Outputs 16-byte aligned.  An E2M1 output in the MMA layout feeds
+ * the next MXFP4 product directly (format-aware fusion for FP4). */
 int mxq_gemm_mx_out(const void* a_q, const uint8_t* a_s, int a_fmt,
                     const void* b_q, const uint8_t* b_s, int b_fmt,
                     int64_t M, int64_t N, int64_t K, int sf_layout,

@@ -109,7 +109,7 @@ def test_argument_checks_need_no_gpu(so):
 
     mo = so.mxq_gemm_mx_out
     row = (FAKE, FAKE, None, None)
-    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 2, 0, 0, *row, None) == -4   # E2M1 output
+    assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 5, 0, 0, *row, None) == -1   # output format
     assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 2, 0, *row, None) == -1   # scale mode
     assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 2, *row, None) == -1   # scale layout
     assert mo(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, 1, 0, 0, 0, FAKE, None, None, None, None) == -1

@@ -23,7 +23,7 @@ from tests.helpers import assert_bytes_equal, f64, np_
 
 pytestmark = pytest.mark.gpu
 
-FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2}
+FMTS = {"e4m3": F.E4M3, "e5m2": F.E5M2, "e2m1": F.E2M1}
 MODES = {"floor": omx.FLOOR, "ceil": omx.CEIL}
 dev = torch.device("cuda")
 
@@ -50,12 +50,12 @@ def run_mx_out(lib, aq, as_, bq, bs, fmt, out_fmt, mode, layout, orientation="ro
         q = q.cpu().numpy()
         s = s.cpu().numpy()
         if layout == "mma":
-            s = omx.sf_from_mma(s.reshape(-1), q.shape[0], q.shape[1] // 32)
+            s = omx.sf_from_mma(s.reshape(-1), q.shape[0], s.size // q.shape[0])
         res += [q, s]
     return res
 
 
-@pytest.mark.parametrize("out_fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("out_fmt", ["e4m3", "e5m2", "e2m1"])
 @pytest.mark.parametrize("mode", ["floor", "ceil"])
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
 @pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 1024), (128, 384, 256)])
@@ -142,6 +142,59 @@ def test_mx_output_exact_mxfp4_operands(lib, orientation, layout, mnk):
     if orientation in ("col", "dual"):
         assert_bytes_equal(cqT, want["q_col"], "column-block codes")
         assert_bytes_equal(csT, want["s_col"], "column-block scales")
+
+
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (256, 512, 512)])
+def test_mxfp4_output_exact_and_feeds_the_next_mxfp4_gemm(lib, layout, mnk):
+    """MXFP4 x MXFP4 product written as MX E2M1 row and column blocks
+    (format-aware fusion for FP4): bit for bit the oracle's quantization of
+    the exact float64 product; the MMA-layout row output is then the A
+    operand of a second MXFP4 product, checked against the oracle too."""
+    M, N, K = mnk
+    rng = np.random.default_rng(31)
+    a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
+    b = rng.integers(-4, 5, (N, K)).astype(np.float64)
+    ra = omx.quantize(a, F.E2M1, omx.ROW, omx.FLOOR)
+    rb = omx.quantize(b, F.E2M1, omx.ROW, omx.FLOOR)
+    aq, as_, bq, bs = ra["q_row"], ra["s_row"], rb["q_row"], rb["s_row"]
+    ref = og.reference(aq, as_, bq, bs, F.E2M1)
+    assert np.array_equal(ref, a @ b.T)
+    want = omx.quantize(ref, F.E2M1, omx.DUAL, omx.FLOOR)
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e2m1", "e2m1", "floor", layout, "dual")
+    assert_bytes_equal(cq, want["q_row"], "E2M1 codes")
+    assert_bytes_equal(cs, want["s_row"], "scales")
+    assert_bytes_equal(cqT, want["q_col"], "E2M1 column-block codes")
+    assert_bytes_equal(csT, want["s_col"], "column-block scales")
+    if layout == "mma" and N % 256 == 0:
+        # the row output [M][N] is the next product's A operand (K' = N)
+        N2 = 256
+        b2 = rng.integers(-2, 3, (N2, N)).astype(np.float64)
+        r2 = omx.quantize(b2, F.E2M1, omx.ROW, omx.FLOOR)
+        out = lib.mx_gemm_mx_out(t(aq), t(omx.sf_to_mma(as_)), t(bq), t(omx.sf_to_mma(bs)), "e2m1",
+                                 out_fmt="e2m1", out_scale_mode="floor", out_sf_layout="mma", orientation="row")
+        c2 = lib.mx_gemm(out[0], out[1], t(r2["q_row"]), t(omx.sf_to_mma(r2["s_row"])), "e2m1", torch.float32)
+        ref2 = og.reference(want["q_row"], want["s_row"], r2["q_row"], r2["s_row"], F.E2M1)
+        assert og.gate_error(c2.cpu().numpy().astype(np.float64), ref2, out_is_bf16=False) <= 1e-5
+
+
+def test_mx_output_e2m1_random_within_one_step(lib):
+    """Random MXFP8 operands, E2M1 output: scales within one binade of the
+    oracle's quantization of the float64 product, and at least 99 % of the
+    codes identical (decisions differ only at rounding boundaries)."""
+    M, N, K = 256, 512, 1024
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    ref = og.reference(aq, as_, bq, bs, F.E4M3)
+    want = omx.quantize(ref, F.E2M1, omx.DUAL, omx.FLOOR)
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e2m1", "floor", "canonical", "dual")
+    for got_q, got_s, wq, ws in ((cq, cs, want["q_row"], want["s_row"]), (cqT, csT, want["q_col"], want["s_col"])):
+        assert np.max(np.abs(got_s.astype(int) - ws.astype(int))) <= 1
+        gn = F.unpack_fp4(got_q)
+        wn = F.unpack_fp4(wq)
+        assert np.mean(gn == wn) >= 0.99
 
 
 def e4m3_spacing(y):
