@@ -488,8 +488,9 @@ def alu_roofline(key: str, elems: int, ms: float, sm_mhz: float):
     instructions it executes per element (profiles/alu.json, from one ncu
     capture of the same kernel source) times the elements per second, against
     the issue peak of the SMs (4 schedulers x 32 lanes, one instruction per
-    clock each, at the maximum SM clock).  None once the kernel source
-    differs from the captured one."""
+    clock each, at the maximum SM clock), with the per-pipe busy fractions of
+    the capture beside it.  None once the kernel source differs from the
+    captured one."""
     p = os.path.join(ROOT, "profiles", "alu.json")
     if not os.path.exists(p):
         return None
@@ -501,9 +502,12 @@ def alu_roofline(key: str, elems: int, ms: float, sm_mhz: float):
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     achieved = e["inst_per_element"] * elems / (ms * 1e-3)
     peak = sms * 128 * sm_mhz * 1e6
-    return {"bound": "alu", "achieved": round(achieved / 1e12, 2), "peak": round(peak / 1e12, 2),
-            "unit": "T thread-instructions/s", "frac": round(achieved / peak, 4),
-            "inst_per_element": e["inst_per_element"], "peak_source": f"{sms} SMs x 128 lanes x {sm_mhz:.0f} MHz"}
+    r = {"bound": "alu", "achieved": round(achieved / 1e12, 2), "peak": round(peak / 1e12, 2),
+         "unit": "T thread-instructions/s", "frac": round(achieved / peak, 4),
+         "inst_per_element": e["inst_per_element"], "peak_source": f"{sms} SMs x 128 lanes x {sm_mhz:.0f} MHz"}
+    if "pipe_busy_pct" in e:
+        r["pipe_busy_pct_ncu"] = e["pipe_busy_pct"]
+    return r
 
 
 def hbm_row(nbytes, ms, hbm, note=None):
