@@ -440,7 +440,20 @@ def fp4_part(args, mxq, X, q, timed, bf16, peak_src, gemm_rows):
                                    "peak_source": f"bf16 burst x {RATIO['e2m1']} ({peak_src})",
                                    "traffic": traffic_for("mx_gemm_pair_kernel", source_sha("gemm.cu"),
                                                           "mxfp4_4096x4096x14336")}})
-    return (ms_q5, ms_q5b, ms_q5c), 4 * args.steps
+    # the same product written as MX E2M1 codes + scales (MMA layout: the
+    # next MXFP4 product's A operand) straight from the accumulator
+    fn6 = lambda: mxq.mx_gemm_mx_out(g5[0], g5[1], b5[0], b5[1], "e2m1", out_fmt="e2m1", out_sf_layout="mma")
+    for _ in range(3):
+        fn6()
+    ms6 = timed(fn6, args.steps)
+    tf6 = gemm_flops(4096, 4096, 14336) / (ms6 * 1e-3) / 1e12
+    gemm_rows.append({"workload": "mxfp4_gemm_mx_e2m1_out_4096x4096x14336", "ms": round(ms6, 4),
+                      "tflops": round(tf6, 1),
+                      "roofline": {"bound": "tensor", "achieved": round(tf6, 1), "peak": round(pk5, 1),
+                                   "unit": "TFLOP/s", "frac": round(tf6 / pk5, 4),
+                                   "peak_source": f"bf16 burst x {RATIO['e2m1']} ({peak_src})",
+                                   "traffic": None}})
+    return (ms_q5, ms_q5b, ms_q5c), 5 * args.steps
 
 
 def pertensor_part(args, mxq, X, timed):
