@@ -418,6 +418,42 @@ def test_full_size_mx_output_sampled(lib):
     assert np.mean(got_codes == wantc["q_row"]) >= 0.99
 
 
+def test_full_size_mx_row_output_sampled(lib):
+    """The bench's MX E4M3 row-output product at full size (the rows-only
+    kernel variant): sampled output rows against the oracle's MX
+    quantization of the float64 product (the property bar)."""
+    M, N, K = 8192, 4096, 4096
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    cq, cs, cqT, _ = run_mx_out(lib, aq, as_, bq, bs, "e4m3", "e4m3", "floor", "mma", "row")
+    assert cqT is None
+    rows = _rows(M, 16, 12)
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E4M3, rows, np.arange(N))
+    want = omx.quantize(ref, F.E4M3, omx.ROW, omx.FLOOR)
+    assert np.max(np.abs(cs[rows].astype(int) - want["s_row"].astype(int))) <= 1
+    assert np.mean(cq[rows] == want["q_row"]) >= 0.99
+
+
+def test_full_size_mxfp4_e2m1_output_sampled(lib):
+    """The bench's MXFP4 product with MX E2M1 output (4096 x 14336 gradient
+    times 4096 x 14336 operand, MMA-layout scales): sampled output rows
+    against the oracle's E2M1 quantization of the float64 product."""
+    M, N, K = 4096, 4096, 14336
+    a = f64(inputs.heavy_gradient(M, K, seed=6))
+    b = f64(inputs.fp4_operand(N, K, seed=8))
+    aq, as_ = mx_operand(a, "e2m1")
+    bq, bs = mx_operand(b, "e2m1")
+    cq, cs, _, _ = run_mx_out(lib, aq, as_, bq, bs, "e2m1", "e2m1", "floor", "mma", "row")
+    assert cq.shape == (M, N // 2)
+    rows = _rows(M, 16, 13)
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E2M1, rows, np.arange(N))
+    want = omx.quantize(ref, F.E2M1, omx.ROW, omx.FLOOR)
+    assert np.max(np.abs(cs[rows].astype(int) - want["s_row"].astype(int))) <= 1
+    assert np.mean(F.unpack_fp4(cq[rows]) == F.unpack_fp4(want["q_row"])) >= 0.99
+
+
 def test_full_size_mm_fp8_sampled(lib):
     """The bench's per-tensor FP8 product at full size and launch
     configuration: 8192 x 4096 E4M3 operand times the transposed view of a
