@@ -6,10 +6,12 @@ replicas under torchrun).
 One step = the dual-orientation MXFP8 quantize workload: 8192 x 4096 bf16
 activations (N(0,1), 0.1 % outlier columns x100) to E4M3 and a same-shape
 gradient (N(0,1e-3)) to E5M2, each with the floor (OCP) and the ceil scale
-rule -- four launches, every one writing the row copy, the transposed column
-copy and both scale arrays (in the GEMM's tensor-core layout).  Each launch
-reads its own input copy (inputs larger than L2: 520 MiB touched per step);
-one CUDA-event pair times each step.  ``value`` is
+rule -- four quantizations, every one writing the row copy, the transposed
+column copy and both scale arrays (in the GEMM's tensor-core layout), run as
+two grouped launches (one per format; the same four as single-tensor calls
+are reported beside them).  Each quantization reads its own input copy
+(inputs larger than L2: 520 MiB touched per step); one CUDA-event pair times
+each step.  ``value`` is
 MX quantize GB/s (algorithmic bytes / kernel time); the same JSON line also
 reports the MXFP8 and MXFP4 GEMMs (TFLOP/s), the per-tensor FP8 step with the
 delayed-scaling fold, the MXFP4 Hadamard + stochastic-rounding quantizer and
@@ -654,21 +656,39 @@ def run_ours(args, rank, world):
                             mxq.SF_MMA, mxq._ptr(qr), mxq._ptr(sr), mxq._ptr(qc), mxq._ptr(sc), stream())
         assert rc == 0, rc
 
+    # the step as the headline runs it: two grouped launches (one per format),
+    # each quantizing its tensor's two copies with floor and ceil scales
+    def group_jobs(idx):
+        jobs = (mxq.QuantJob * len(idx))()
+        for k, i in enumerate(idx):
+            x, fmt, mode = runs[i]
+            qr, sr, qc, sc = outs[i]
+            jobs[k] = mxq.QuantJob(x.data_ptr(), M, K, K, mxq._SCALE[mode], qr.data_ptr(), sr.data_ptr(),
+                                   qc.data_ptr(), sc.data_ptr())
+        return jobs
+    groups = [(group_jobs([0, 1]), "e4m3"), (group_jobs([2, 3]), "e5m2")]
+
+    def launch_group(g):
+        jobs, fmt = groups[g]
+        rc = L.mxq_quantize_group(jobs, len(jobs), mxq._FMT[fmt], mxq.DUAL, mxq.SF_MMA, stream())
+        assert rc == 0, rc
+
     # clocks are sampled from the warm-up through the last timed launch
     sampler = ClockSampler(local)
     sampler.start()
     # ---------------- warmup
     for _ in range(args.warmup):
+        for g in range(2):
+            launch_group(g)
         for i in range(4):
             launch_quant(i)
     torch.cuda.synchronize()
 
-    # ---------------- timed region: K steps of 4 quantize launches
+    # ---------------- timed region: K steps of 2 grouped quantize launches
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    per_launch = []
     st = torch.cuda.current_stream(dev)
     evs = []
     torch.cuda._sleep(HOST_LEAD_CYCLES)
@@ -676,8 +696,8 @@ def run_ours(args, rank, world):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(st)
-        for i in range(4):
-            launch_quant(i)
+        for g in range(2):
+            launch_group(g)
             launches += 1
         b.record(st)
         evs.append((a, b))
@@ -687,16 +707,29 @@ def run_ours(args, rank, world):
     wall = time.perf_counter() - t_wall
     per_step = [a.elapsed_time(b) for a, b in evs]
     ms_step = statistics.mean(per_step)
-    per_launch = [t / 4 for t in per_step]
-    # for reference: one launch alone after an L2 flush (write + read-back)
+    per_launch = [t / 2 for t in per_step]
+    # the same step as four single-tensor calls (mxq_quantize), timed the same way
+    evs1 = []
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for i in range(4):
+            launch_quant(i)
+        b.record(st)
+        evs1.append((a, b))
+    torch.cuda.synchronize()
+    ms_step_single = statistics.mean(a.elapsed_time(b) for a, b in evs1)
+    # for reference: one single-tensor launch alone after an L2 flush (write + read-back)
     iso_ms = timed(lambda: launch_quant(0), 20)
-    launch_detail = {"headline_steps": launches, "headline_isolated": 20}
-    launches += 20
+    launch_detail = {"headline_steps": launches, "single_call_steps": 4 * args.steps, "headline_isolated": 20}
+    launches += 4 * args.steps + 20
     ms_step = max_over_ranks(ms_step, world, dev)
     step_bytes = 4 * mx_quant_bytes(M, K)
     value = weak_scaling_value(step_bytes, world, ms_step)
     launch_ms = statistics.mean(per_launch)
-    ach = mx_quant_bytes(M, K) / (launch_ms * 1e-3) / 1e9
+    ach = 2 * mx_quant_bytes(M, K) / (launch_ms * 1e-3) / 1e9          # a launch quantizes two tensors
 
     gemm_rows, ms3, ms_q5, ms1q, ms1d = [], None, None, None, None
     b3 = pertensor_bytes(4096, 14336)
@@ -716,7 +749,8 @@ def run_ours(args, rank, world):
     clocks = sampler.stop()
     if args.case != "all":
         if rank == 0:
-            print(json.dumps({"case": args.case, "quant_ms_per_step": ms_step, "gemm": gemm_rows, "pertensor_ms": ms3,
+            print(json.dumps({"case": args.case, "quant_ms_per_step": ms_step,
+                              "quant_ms_per_step_single_calls": ms_step_single, "gemm": gemm_rows, "pertensor_ms": ms3,
                               "fp4_quant_ms": ms_q5, "small_us": [ms1q, ms1d], "clocks": clocks}), flush=True)
         return 0
     # ---------------- e2e through the public API: host buffers, copies inside
@@ -779,16 +813,20 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "ms_per_step_median": round(statistics.median(per_step), 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic (seeded numpy, rounded to bf16)",
-        "config": {"workload": WORKLOAD, "rows": M, "cols": K, "launches_per_step": 4,
-                   "l2": ("inputs larger than L2: each launch of a step reads its own 64 MiB input copy and "
+        "config": {"workload": WORKLOAD, "rows": M, "cols": K, "launches_per_step": 2,
+                   "grouping": ("two mxq_quantize_group launches per step, E4M3 [floor, ceil] on the activations' "
+                                "two copies and E5M2 [floor, ceil] on the gradients' two copies; the same bytes as "
+                                "four mxq_quantize calls (reported under rows.dual_quantize_step_four_single_calls)"),
+                   "l2": ("inputs larger than L2: each quantize of a step reads its own 64 MiB input copy and "
                           "writes its own outputs (520 MiB per step, 4x the 129 MB L2); one event pair per step"),
                    "bytes_per_step": step_bytes,
                    "isolated_launch_us": round(iso_ms * 1e3, 2),
                    "isolated_launch_note": "one launch after an L2 flush (256 MiB written then read back), event-timed"},
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(ach / hbm, 4), "peak_source": f"hbm_gbs ({peak_src})",
-                     "traffic": traffic_for("quant_tiles_kernel", source_sha("quantize.cu"), "dual_e4m3_floor_8192x4096"),
-                     "algorithmic_bytes_per_launch": mx_quant_bytes(M, K)},
+                     "traffic": traffic_for("quant_tiles_kernel", source_sha("quantize.cu"),
+                                            "group_dual_e4m3_floor_ceil_8192x4096"),
+                     "algorithmic_bytes_per_launch": 2 * mx_quant_bytes(M, K)},
         "clocks": clocks,
         "e2e": {"value": round(step_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3),
@@ -799,6 +837,9 @@ def run_ours(args, rank, world):
         "gpu_launches_detail": launch_detail,
         "gemm": {"metric": "MX GEMM TFLOP/s", "rows": gemm_rows, "cpu_baseline": gcpu},
         "rows": {
+            "dual_quantize_step_four_single_calls": dict(
+                hbm_row(step_bytes, ms_step_single, hbm, "the headline step as four mxq_quantize launches"),
+                ms_per_launch=round(ms_step_single / 4, 4)),
             "pertensor_fp8_ring_4096x14336_dual": hbm_row(b3, ms3[0], hbm),
             "pertensor_fp8_ring_4096x14336_transposed": hbm_row(pertensor_bytes(4096, 14336, "col"), ms3[1], hbm),
             "mxfp4_hadamard_sr_quantize_4096x14336": dict(hbm_row(
@@ -817,7 +858,8 @@ def run_ours(args, rank, world):
     # a compact copy of every row's time and roofline fraction, last on the
     # line so that a reader who keeps only its tail still has all of them
     line["summary"] = {
-        "headline": {"us_per_launch": round(launch_ms * 1e3, 2), "frac": line["roofline"]["frac"]},
+        "headline": {"us_per_launch": round(launch_ms * 1e3, 2), "launches_per_step": 2,
+                     "frac": line["roofline"]["frac"]},
         "gemm": {r["workload"]: [r["ms"], r["roofline"]["frac"]] for r in gemm_rows},
         "quant": {k: [v["ms"], v["roofline"]["frac"]] for k, v in line["rows"].items() if "ms" in v},
         "cpu_gbs": {"one_core": round(cpu["value"], 4), "all_cores": round(cpu["all_cores"]["value"], 4),

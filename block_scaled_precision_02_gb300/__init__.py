@@ -37,6 +37,16 @@ _SF = {"canonical": SF_CANONICAL, "mma": SF_MMA, SF_CANONICAL: SF_CANONICAL, SF_
 _lib = None
 
 
+QUANT_GROUP_MAX = 4   # MXQ_QUANT_GROUP_MAX
+
+
+class QuantJob(ctypes.Structure):
+    """One job of mxq_quantize_group (the C struct mxq_quant_job)."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ld", ctypes.c_int64), ("scale_mode", ctypes.c_int), ("q_row", ctypes.c_void_p),
+                ("s_row", ctypes.c_void_p), ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
+
+
 class MXQError(RuntimeError):
     def __init__(self, status: int, what: str):
         msg = _lib.mxq_strerror(status).decode() if _lib is not None else str(status)
@@ -55,6 +65,7 @@ def load() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
     L.mxq_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, i32, i32, u64, u64, i32, vp, vp, vp, vp, vp]
+    L.mxq_quantize_group.argtypes = [ctypes.POINTER(QuantJob), i32, i32, i32, i32, vp]
     L.mxq_dequantize.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
     L.fp8_quantize_pertensor.argtypes = [vp, i64, i64, vp, i32, i32, vp, i32, i32, f32, f32, vp, vp, vp, vp]
     L.fp8_ring_fold.argtypes = [vp, vp, i32, i32, f32, f32, vp]
@@ -71,7 +82,7 @@ def load() -> ctypes.CDLL:
     L.mxq_strerror.restype = ctypes.c_char_p
     L.mxq_version.argtypes = []
     L.mxq_test_stall_next_launch.argtypes = [i32]
-    for name in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
+    for name in ("mxq_quantize", "mxq_quantize_group", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
                  "mxq_gemm_mixed", "mxq_gemm_workspace_size", "mxq_gemm_ws", "mxq_gemm_noalloc",
                  "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
                  "mxq_last_device_status", "mxq_version", "mxq_test_stall_next_launch"):
@@ -187,6 +198,44 @@ def mx_quantize(x: torch.Tensor, fmt="e4m3", orientation="row", scale_mode="floo
           int(bool(hadamard32)), sr_key & (2**64 - 1), hadamard_seed & (2**64 - 1), _SF[sf_layout], _ptr(q_row),
           _ptr(s_row), _ptr(q_col), _ptr(s_col))
     return q_row, s_row, q_col, s_col
+
+
+def mx_quantize_group(xs, fmt="e4m3", orientation="row", scale_modes="floor", sf_layout="canonical"):
+    """MX-quantize up to QUANT_GROUP_MAX bf16 tensors of one format and
+    orientation (RNE, no Hadamard) in one launch: the persistent grid runs
+    through all of them, so the fill and drain of a launch are paid once.
+    ``scale_modes`` is one mode for all tensors or a sequence, one per tensor.
+    Returns one (q_row, s_row, q_col, s_col) tuple per tensor, each exactly
+    what mx_quantize returns for it."""
+    xs = list(xs)
+    if not 1 <= len(xs) <= QUANT_GROUP_MAX:
+        raise ValueError(f"between 1 and {QUANT_GROUP_MAX} tensors per group")
+    modes = [scale_modes] * len(xs) if isinstance(scale_modes, str) else list(scale_modes)
+    if len(modes) != len(xs):
+        raise ValueError("one scale mode, or one per tensor")
+    f, o = _FMT[fmt], _ORIENT[orientation]
+    qb = 2 if f == E2M1 else 1
+    dev = None
+    outs, jobs = [], (QuantJob * len(xs))()
+    for k, (x, mode) in enumerate(zip(xs, modes)):
+        _cuda_2d(x, f"xs[{k}]")
+        if x.dtype != torch.bfloat16 or x.stride(1) != 1:
+            raise ValueError("every tensor must be bf16 with a contiguous last dimension")
+        dev = x.device if dev is None else dev
+        _on_device(((x, f"xs[{k}]"),), dev)
+        rows, cols = x.shape
+        q_row = s_row = q_col = s_col = None
+        if o & ROW:
+            q_row = torch.empty(rows, cols // qb, dtype=torch.uint8, device=dev)
+            s_row = torch.empty(rows, cols // 32, dtype=torch.uint8, device=dev)
+        if o & COL:
+            q_col = torch.empty(cols, rows // qb, dtype=torch.uint8, device=dev)
+            s_col = torch.empty(cols, rows // 32, dtype=torch.uint8, device=dev)
+        jobs[k] = QuantJob(x.data_ptr(), rows, cols, x.stride(0), _SCALE[mode],
+                           *[0 if t is None else t.data_ptr() for t in (q_row, s_row, q_col, s_col)])
+        outs.append((q_row, s_row, q_col, s_col))
+    _call("mxq_quantize_group", dev, jobs, len(xs), f, o, _SF[sf_layout])
+    return outs
 
 
 def mx_dequantize(q: torch.Tensor, s: torch.Tensor, fmt="e4m3", out_dtype=torch.float32) -> torch.Tensor:

@@ -314,12 +314,36 @@ __device__ __forceinline__ void fold_ring(volatile float* ring, int n, int hist_
   reinterpret_cast<volatile unsigned int*>(ring)[n + 3] = 0u;
 }
 
+// The tensors of one launch: NJ quantize jobs of one format and orientation
+// (NJ = 1: a single tensor).  Their tiles form one sequence in job order: job
+// j owns tiles tile_end[j - 1] .. tile_end[j] - 1 (tile_end[-1] = 0), so the
+// persistent CTAs run through all jobs without a launch boundary between
+// them.  Unused trailing entries repeat the total in tile_end.  Job 0's
+// parameters also travel as a separate by-value kernel argument, which is
+// all a single-tensor launch reads (plain parameter loads).
+template <int NJ>
+struct QuantLaunch {
+  CUtensorMap mx[NJ];        // bf16 input boxes
+  CUtensorMap mr[NJ];        // row-block codes
+  CUtensorMap mc[NJ];        // transposed column-block codes
+  QuantParams p[NJ];
+  int tile_end[NJ];
+};
+
+// Job of a tile of the launch: the number of jobs that end at or before it.
+template <int NJ>
+__device__ __forceinline__ int job_of(const QuantLaunch<NJ>& L, int tile) {
+  int j = 0;
+#pragma unroll
+  for (int k = 0; k + 1 < NJ; ++k) j += tile >= L.tile_end[k] ? 1 : 0;
+  return j;
+}
+
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
-template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT>
+template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT, int NJ>
 __global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA>::MIN_BLOCKS)
-quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_qrow,
-                   const __grid_constant__ CUtensorMap map_qcol, const QuantParams p) {
+quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams p0) {
   using T = TileCfg<NSTG, NOUT, EXTRA>;
   constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
@@ -345,17 +369,28 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red + T::NW);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t signs = (EXTRA && p.hadamard) ? hadamard_sign_mask(p.had_k0, p.had_k1) : 0u;
+  // p0: job 0, and what all jobs share (status, rounding, per-tensor state)
+  const int ntiles = NJ == 1 ? p0.ntiles : L.tile_end[NJ - 1];
+  const uint32_t signs = (EXTRA && p0.hadamard) ? hadamard_sign_mask(p0.had_k0, p0.had_k1) : 0u;
+  // first tile row and column of a tile of the launch, in its job's tensor
+  auto tile_origin = [&](int tile, int jb, int& r0, int& c0) {
+    const QuantParams& pj = NJ == 1 ? p0 : L.p[jb];
+    const int t = tile - (jb ? L.tile_end[jb - 1] : 0);
+    r0 = (t / pj.tiles_c) * TR;
+    c0 = (t % pj.tiles_c) * TC;
+  };
 
   // Load of this CTA's tile i into its stage (issued by one thread).
   auto issue = [&](int i) {
     const int tile = blockIdx.x + i * gridDim.x;
-    if (tile == p.stall_tile) return;      // test hook: leave this stage's phase incomplete
-    const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
+    if (tile == p0.stall_tile) return;     // test hook: leave this stage's phase incomplete
+    const int jb = job_of(L, tile);
+    int r0, c0;
+    tile_origin(tile, jb, r0, c0);
     const uint32_t bar = smem_u32(&bars[i % NSTG]);
     last_use[i % NSTG] = i;
     mbar_arrive_expect_tx(bar, T::IN_BYTES);
-    tma_load_2d(smem_u32(in_s + (i % NSTG) * T::IN_BYTES), &map_x, bar, c0, r0);
+    tma_load_2d(smem_u32(in_s + (i % NSTG) * T::IN_BYTES), &L.mx[jb], bar, c0, r0);
   };
 
   if (tid == 0) {
@@ -366,25 +401,33 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     }
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&map_x);
-    if (DO_ROW) prefetch_tensormap(&map_qrow);
-    if (DO_COL) prefetch_tensormap(&map_qcol);
+#pragma unroll
+    for (int k = 0; k < NJ; ++k) {
+      prefetch_tensormap(&L.mx[k]);
+      if (DO_ROW) prefetch_tensormap(&L.mr[k]);
+      if (DO_COL) prefetch_tensormap(&L.mc[k]);
+    }
     // The first tiles' input into L2 while the previous kernel in the stream
     // may still be finishing.  L2 is where the GPU's memory is coherent: a
     // write of that kernel that lands later updates the prefetched line, and
     // the loads below are issued only after grid_dep_wait, so they see it.
     for (int i = 0; i < NSTG; ++i) {
       const int tile = blockIdx.x + i * gridDim.x;
-      if (tile < p.ntiles) tma_prefetch_2d(&map_x, (tile % p.tiles_c) * TC, (tile / p.tiles_c) * TR);
+      if (tile < ntiles) {
+        const int jb = job_of(L, tile);
+        int r0, c0;
+        tile_origin(tile, jb, r0, c0);
+        tma_prefetch_2d(&L.mx[jb], c0, r0);
+      }
     }
   }
   __syncthreads();
   grid_dep_launch();
   grid_dep_wait();                 // before any other global-memory access
-  const float mult = PERTENSOR ? *p.scale : 1.0f;
+  const float mult = PERTENSOR ? *p0.scale : 1.0f;
   if (tid == 0) {
     for (int i = 0; i < NSTG; ++i)
-      if (blockIdx.x + i * gridDim.x < p.ntiles) issue(i);
+      if (blockIdx.x + i * gridDim.x < ntiles) issue(i);
   }
 
   // This warp's part of every tile.
@@ -397,8 +440,11 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   if (row_warp || col_warp) {
     for (int i = 0;; ++i) {
       const int tile = blockIdx.x + i * gridDim.x;
-      if (tile >= p.ntiles || *abort_flag) break;
-      const int r0 = (tile / p.tiles_c) * TR, c0 = (tile % p.tiles_c) * TC;
+      if (tile >= ntiles || *abort_flag) break;
+      const int jb = job_of(L, tile);
+      const QuantParams& p = NJ == 1 ? p0 : L.p[jb];   // this tile's tensor
+      int r0, c0;
+      tile_origin(tile, jb, r0, c0);
       const int s = i % NSTG;
       if (!mbar_wait(smem_u32(&bars[s]), (i / NSTG) & 1, p.status)) {
         *abort_flag = 1;
@@ -468,7 +514,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&map_qrow, smem_u32(stg), FP4 ? c0 / 2 : c0, r0 + ro);
+          tma_store_2d(&L.mr[jb], smem_u32(stg), FP4 ? c0 / 2 : c0, r0 + ro);
           bulk_commit();
         }
         // row scales: the lane's BPL bytes (blocks b0 .. b0 + BPL - 1 of its row)
@@ -545,7 +591,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&map_qcol, smem_u32(stg), FP4 ? (r0 + 32 * rb) / 2 : r0 + 32 * rb, c0);
+          tma_store_2d(&L.mc[jb], smem_u32(stg), FP4 ? (r0 + 32 * rb) / 2 : r0 + 32 * rb, c0);
           bulk_commit();
         }
         // column scales: one byte per column of the lane for this band
@@ -574,7 +620,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       // release the stage; the last of its readers issues its next load
       if (lane == 0) {
         const uint32_t old = atomicAdd(&cnt[s], 1u);
-        if (old % ACTIVE == static_cast<uint32_t>(ACTIVE - 1) && blockIdx.x + (i + NSTG) * gridDim.x < p.ntiles)
+        if (old % ACTIVE == static_cast<uint32_t>(ACTIVE - 1) && blockIdx.x + (i + NSTG) * gridDim.x < ntiles)
           issue(i + NSTG);
       }
     }
@@ -586,7 +632,7 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   if (tid == 0 && *abort_flag) {
     // a wait gave up: let every load still in flight land before the CTA ends
     for (int st = 0; st < NSTG; ++st)
-      if (last_use[st] >= 0) (void)mbar_wait(smem_u32(&bars[st]), (last_use[st] / NSTG) & 1, p.status);
+      if (last_use[st] >= 0) (void)mbar_wait(smem_u32(&bars[st]), (last_use[st] / NSTG) & 1, p0.status);
   }
 
   if constexpr (PERTENSOR) {
@@ -598,11 +644,11 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
     if (tid == 0) {
       uint32_t m = 0;
       for (int k = 0; k < T::NW; ++k) m = max(m, red[k]);
-      const int n = p.hist_len;
-      if (p.ring == nullptr) {
-        atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), m);
+      const int n = p0.hist_len;
+      if (p0.ring == nullptr) {
+        atomicMax(reinterpret_cast<unsigned int*>(p0.amax_out), m);
       } else {
-        float* ring = p.ring;
+        float* ring = p0.ring;
         atomicMax(reinterpret_cast<unsigned int*>(ring + n + 2), m);
         __threadfence();
         const unsigned int ticket = atomicAdd(reinterpret_cast<unsigned int*>(ring + n + 3), 1u);
@@ -610,8 +656,8 @@ quant_tiles_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
           __threadfence();
           volatile float* vr = ring;
           const float amax = vr[n + 2];
-          if (p.amax_out) *p.amax_out = amax;
-          fold_ring(vr, n, p.hist_idx, amax, p.fp8_max, p.margin);
+          if (p0.amax_out) *p0.amax_out = amax;
+          fold_ring(vr, n, p0.hist_idx, amax, p0.fp8_max, p0.margin);
           __threadfence();
         }
       }
@@ -717,11 +763,10 @@ constexpr int QTC = TileCfg<1, 1, false>::TC;
 constexpr int QNST = MXQ_QUANT_NST;
 constexpr int QSTG = MXQ_QUANT_STG;
 
-template <int FMT, int ORIENT, bool PT, bool EXTRA>
-int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc, const QuantParams& p,
-                 cudaStream_t st) {
+template <int FMT, int ORIENT, bool PT, bool EXTRA, int NJ>
+int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
   using T = TileCfg<QNST, QSTG, EXTRA>;
-  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG>;
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
   static int per_sm[64] = {};
@@ -738,20 +783,25 @@ int launch_tiles(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap
   // as many rounds of tiles as the resident CTAs need, spread evenly over
   // the fewest CTAs that take them in that many rounds: every CTA then works
   // until the last round (the tail is at most one tile per CTA shorter)
+  const int ntiles = L.tile_end[NJ - 1];
   const int slots = per_sm[dev & 63] * sm_count();
-  const int rounds = (p.ntiles + slots - 1) / slots;
-  const int grid = (p.ntiles + rounds - 1) / rounds;
-  return launch_pdl(kern, dim3(grid), dim3(T::THREADS), smem, st, mx, mr, mc, p);
+  const int rounds = (ntiles + slots - 1) / slots;
+  const int grid = (ntiles + rounds - 1) / rounds;
+  return launch_pdl(kern, dim3(grid), dim3(T::THREADS), smem, st, L, L.p[0]);
 }
 
-template <bool PT>
-int dispatch(int fmt, int orient, const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc,
-             const QuantParams& p, cudaStream_t st) {
-  const bool extra = !PT && (p.rounding != MXQ_RNE || p.hadamard);
+// A launch of one tensor (NJ = 1: every variant), or a group of RNE jobs
+// (NJ > 1: the lean variants only).
+template <bool PT, int NJ>
+int dispatch(int fmt, int orient, const QuantLaunch<NJ>& L, cudaStream_t st) {
+  const bool extra = !PT && (L.p[0].rounding != MXQ_RNE || L.p[0].hadamard);
+  if (NJ > 1 && (PT || extra)) return MXQ_ERR_UNSUPPORTED;
 #define MXQ_CASE(F, O)                                                                  \
-  if (fmt == F && orient == O)                                                          \
-    return extra ? launch_tiles<F, O, PT, !PT>(mx, mr, mc, p, st)                      \
-                 : launch_tiles<F, O, PT, false>(mx, mr, mc, p, st);
+  if (fmt == F && orient == O) {                                                        \
+    if constexpr (NJ > 1) return launch_tiles<F, O, false, false, NJ>(L, st);          \
+    else return extra ? launch_tiles<F, O, PT, !PT, 1>(L, st)                          \
+                      : launch_tiles<F, O, PT, false, 1>(L, st);                       \
+  }
   MXQ_CASE(MXQ_E4M3, MXQ_ROW) MXQ_CASE(MXQ_E4M3, MXQ_COL) MXQ_CASE(MXQ_E4M3, MXQ_DUAL)
   MXQ_CASE(MXQ_E5M2, MXQ_ROW) MXQ_CASE(MXQ_E5M2, MXQ_COL) MXQ_CASE(MXQ_E5M2, MXQ_DUAL)
   if constexpr (!PT) {
@@ -797,15 +847,12 @@ int make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, bool fp4, i
   return MXQ_OK;
 }
 
-}  // namespace
-
-extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int orient,
-                            int scale_mode, int rounding, int hadamard32, uint64_t sr_key,
-                            uint64_t hadamard_seed, int sf_layout, void* q_row, uint8_t* s_row, void* q_col,
-                            uint8_t* s_col, void* stream) {
-  if (!x || !valid_fmt(fmt) || !valid_orient(orient)) return MXQ_ERR_BAD_ARG;
+// Argument checks of one MX quantize of x [rows][cols] (row stride ld
+// elements); the format and orientation are checked by the caller.
+int check_mx_args(const void* x, int64_t rows, int64_t cols, int64_t ld, int orient, int scale_mode, int sf_layout,
+                  const void* q_row, const uint8_t* s_row, const void* q_col, const uint8_t* s_col) {
+  if (!x) return MXQ_ERR_BAD_ARG;
   if (scale_mode != MXQ_SCALE_FLOOR_OCP && scale_mode != MXQ_SCALE_CEIL) return MXQ_ERR_BAD_ARG;
-  if (rounding != MXQ_RNE && rounding != MXQ_SR && rounding != MXQ_SR4) return MXQ_ERR_BAD_ARG;
   if (sf_layout != MXQ_SF_CANONICAL && sf_layout != MXQ_SF_MMA) return MXQ_ERR_BAD_ARG;
   if ((orient & MXQ_ROW) && (!q_row || !s_row)) return MXQ_ERR_BAD_ARG;
   if ((orient & MXQ_COL) && (!q_col || !s_col)) return MXQ_ERR_BAD_ARG;
@@ -817,12 +864,28 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   if ((orient & MXQ_COL) && !aligned16(q_col)) return MXQ_ERR_MISALIGNED;
   if (sf_layout == MXQ_SF_MMA && (((orient & MXQ_ROW) && !aligned16(s_row)) || ((orient & MXQ_COL) && !aligned16(s_col))))
     return MXQ_ERR_MISALIGNED;
+  return MXQ_OK;
+}
+
+// Tiles of one tensor: 128-row x 64-column boxes, ragged edges included.
+int64_t tile_count(int64_t rows, int64_t cols) { return ((cols + QTC - 1) / QTC) * ((rows + TR - 1) / TR); }
+
+}  // namespace
+
+extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int orient,
+                            int scale_mode, int rounding, int hadamard32, uint64_t sr_key,
+                            uint64_t hadamard_seed, int sf_layout, void* q_row, uint8_t* s_row, void* q_col,
+                            uint8_t* s_col, void* stream) {
+  if (!valid_fmt(fmt) || !valid_orient(orient)) return MXQ_ERR_BAD_ARG;
+  if (rounding != MXQ_RNE && rounding != MXQ_SR && rounding != MXQ_SR4) return MXQ_ERR_BAD_ARG;
+  const int rc0 = check_mx_args(x, rows, cols, ld, orient, scale_mode, sf_layout, q_row, s_row, q_col, s_col);
+  if (rc0) return rc0;
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
 
-  CUtensorMap mx, mr, mc;
-  int rc = make_maps(x, rows, cols, ld, fmt == MXQ_E2M1, orient, q_row, q_col, &mx, &mr, &mc);
+  QuantLaunch<1> L{};
+  int rc = make_maps(x, rows, cols, ld, fmt == MXQ_E2M1, orient, q_row, q_col, &L.mx[0], &L.mr[0], &L.mc[0]);
   if (rc) return rc;
-  QuantParams p{};
+  QuantParams& p = L.p[0];
   p.rows = static_cast<int>(rows);
   p.cols = static_cast<int>(cols);
   p.tiles_c = static_cast<int>((cols + QTC - 1) / QTC);
@@ -840,7 +903,57 @@ extern "C" int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   p.status = status_ptr();
   p.stall_tile = take_test_stall(1) ? 0 : -1;
   if (!p.status) return MXQ_ERR_CUDA;
-  return dispatch<false>(fmt, orient, mx, mr, mc, p, static_cast<cudaStream_t>(stream));
+  L.tile_end[0] = p.ntiles;
+  return dispatch<false>(fmt, orient, L, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mxq_quantize_group(const mxq_quant_job* jobs, int njobs, int fmt, int orient, int sf_layout,
+                                  void* stream) {
+  if (!jobs || njobs < 1 || njobs > MXQ_QUANT_GROUP_MAX || !valid_fmt(fmt) || !valid_orient(orient))
+    return MXQ_ERR_BAD_ARG;
+  int64_t total = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const mxq_quant_job& J = jobs[j];
+    const int rc = check_mx_args(J.x, J.rows, J.cols, J.ld, orient, J.scale_mode, sf_layout, J.q_row, J.s_row,
+                                 J.q_col, J.s_col);
+    if (rc) return rc;
+    total += tile_count(J.rows, J.cols);
+  }
+  if (total > (1ll << 31) - 1) return MXQ_ERR_BAD_SHAPE;
+  if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return MXQ_ERR_CUDA;
+  QuantLaunch<MXQ_QUANT_GROUP_MAX> L{};
+  int end = 0;
+  for (int j = 0; j < MXQ_QUANT_GROUP_MAX; ++j) {
+    if (j >= njobs) {                          // unused: never reached (its tiles end where the last job's do)
+      L.mx[j] = L.mx[0];
+      L.mr[j] = L.mr[0];
+      L.mc[j] = L.mc[0];
+      L.p[j] = L.p[0];
+      L.tile_end[j] = end;
+      continue;
+    }
+    const mxq_quant_job& J = jobs[j];
+    const int rc = make_maps(J.x, J.rows, J.cols, J.ld, fmt == MXQ_E2M1, orient, J.q_row, J.q_col, &L.mx[j],
+                             &L.mr[j], &L.mc[j]);
+    if (rc) return rc;
+    QuantParams& p = L.p[j];
+    p.rows = static_cast<int>(J.rows);
+    p.cols = static_cast<int>(J.cols);
+    p.tiles_c = static_cast<int>((J.cols + QTC - 1) / QTC);
+    p.ntiles = static_cast<int>(tile_count(J.rows, J.cols));
+    p.ceil_mode = J.scale_mode == MXQ_SCALE_CEIL;
+    p.rounding = MXQ_RNE;
+    p.sf_mma = sf_layout == MXQ_SF_MMA;
+    p.s_row = J.s_row;
+    p.s_col = J.s_col;
+    p.status = status;
+    p.stall_tile = -1;
+    end += p.ntiles;
+    L.tile_end[j] = end;
+  }
+  return dispatch<false>(fmt, orient, L, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols, const float* scale, int fmt,
@@ -860,10 +973,10 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
   if (!device_ok()) return MXQ_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  CUtensorMap mx, mr, mc;
-  int rc = make_maps(x, rows, cols, cols, false, orient, x8, x8T, &mx, &mr, &mc);
+  QuantLaunch<1> L{};
+  int rc = make_maps(x, rows, cols, cols, false, orient, x8, x8T, &L.mx[0], &L.mr[0], &L.mc[0]);
   if (rc) return rc;
-  QuantParams p{};
+  QuantParams& p = L.p[0];
   p.rows = static_cast<int>(rows);
   p.cols = static_cast<int>(cols);
   p.tiles_c = static_cast<int>((cols + QTC - 1) / QTC);
@@ -881,7 +994,8 @@ extern "C" int fp8_quantize_pertensor(const void* x, int64_t rows, int64_t cols,
   if (!ring_state) {
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return MXQ_ERR_CUDA;
   }
-  return dispatch<true>(fmt, orient, mx, mr, mc, p, st);
+  L.tile_end[0] = p.ntiles;
+  return dispatch<true>(fmt, orient, L, st);
 }
 
 extern "C" int fp8_ring_fold(const float* amax, float* ring_state, int hist_len, int hist_idx, float fp8_max,

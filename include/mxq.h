@@ -123,6 +123,34 @@ int mxq_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
                  int sf_layout, void* q_row, uint8_t* s_row, void* q_col,
                  uint8_t* s_col, void* stream);
 
+/* ---- Grouped MX quantize (no counterpart in the pages: a batching of
+ * mxq_quantize) --------------------------------------------------------------
+ * Up to MXQ_QUANT_GROUP_MAX tensors of one format and orientation, RNE
+ * elements, no Hadamard, quantized in one launch: the tiles of all jobs form
+ * one sequence that the persistent grid runs through, so the fill and drain
+ * of a launch are paid once for the group instead of once per tensor.  Each
+ * job's bytes are exactly those mxq_quantize(job.x, ..., fmt, orient,
+ * job.scale_mode, MXQ_RNE, 0, 0, 0, sf_layout, ...) writes.
+ * jobs     host array of njobs descriptions (read during the call only);
+ *          every field as the same argument of mxq_quantize, all device
+ *          pointers on the current device.
+ * njobs    1 .. MXQ_QUANT_GROUP_MAX.
+ * Errors: any job's argument error is returned as mxq_quantize would return
+ * it, before anything is launched.  Outputs of different jobs must not
+ * overlap one another or any input. */
+#define MXQ_QUANT_GROUP_MAX 4
+typedef struct mxq_quant_job {
+  const void* x;               /* bf16 [rows][ld] */
+  int64_t rows, cols, ld;
+  int scale_mode;              /* MXQ_SCALE_FLOOR_OCP | MXQ_SCALE_CEIL */
+  void* q_row;                 /* ROW / DUAL outputs (else NULL) */
+  uint8_t* s_row;
+  void* q_col;                 /* COL / DUAL outputs (else NULL) */
+  uint8_t* s_col;
+} mxq_quant_job;
+int mxq_quantize_group(const mxq_quant_job* jobs, int njobs, int fmt,
+                       int orient, int sf_layout, void* stream);
+
 /* ---- MX dequantize ([MX] section 1: V_i ~= q_i * X) --------------------------
  * q        codes [rows][cols] (E2M1 packed [rows][cols/2]), s canonical
  *          scales [rows][cols/32].  out [rows][cols]: float32 when

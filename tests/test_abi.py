@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_quantize", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold", "mxq_gemm",
+    for n in ("mxq_quantize", "mxq_quantize_group", "mxq_dequantize", "fp8_quantize_pertensor", "fp8_ring_fold",
+              "mxq_gemm",
               "mxq_gemm_mixed", "mxq_gemm_ws", "mxq_gemm_workspace_size",
               "mxq_gemm_mx_out", "mxq_mm_fp8", "mxq_sf_to_mma",
               "mxq_last_device_status", "mxq_strerror", "mxq_version"):
@@ -160,3 +161,28 @@ def test_product_path_never_imports_the_oracle():
         if path.endswith((".py", ".cu", ".cuh", ".h")):
             text = open(path).read()
             assert "import oracle" not in text and "from oracle" not in text, path
+
+
+def test_group_argument_checks_need_no_gpu(so):
+    """mxq_quantize_group: the group's own checks, then each job's, in job
+    order, all before any launch (on a machine without a GPU the last step
+    is the device check)."""
+    from block_scaled_precision_02_gb300 import QuantJob
+    g = so.mxq_quantize_group
+    ok = QuantJob(0x10000, 64, 64, 64, 0, 0x10000, 0x10000, 0, 0)
+    jobs = (QuantJob * 5)(ok, ok, ok, ok, ok)
+    assert g(None, 1, 0, 1, 0, None) == -1                       # no jobs array
+    assert g(jobs, 0, 0, 1, 0, None) == -1                       # empty group
+    assert g(jobs, 5, 0, 1, 0, None) == -1                       # more than MXQ_QUANT_GROUP_MAX
+    assert g(jobs, 2, 9, 1, 0, None) == -1                       # format
+    assert g(jobs, 2, 0, 4, 0, None) == -1                       # orientation
+    assert g(jobs, 2, 0, 1, 5, None) == -1                       # scale layout
+    bad = (QuantJob * 2)(ok, QuantJob(0x10000, 48, 64, 64, 0, 0x10000, 0x10000, 0, 0))
+    assert g(bad, 2, 0, 1, 0, None) == -2                        # the second job's shape
+    bad = (QuantJob * 2)(ok, QuantJob(0x10000, 64, 64, 64, 2, 0x10000, 0x10000, 0, 0))
+    assert g(bad, 2, 0, 1, 0, None) == -1                        # the second job's scale mode
+    bad = (QuantJob * 2)(QuantJob(0x10008, 64, 64, 64, 0, 0x10000, 0x10000, 0, 0), ok)
+    assert g(bad, 2, 0, 1, 0, None) == -3                        # the first job's input alignment
+    bad = (QuantJob * 1)(QuantJob(0x10000, 64, 64, 64, 0, 0x10000, 0x10000, 0, 0))
+    assert g(bad, 1, 0, 3, 0, None) == -1                        # DUAL without column outputs
+    assert g(jobs, 4, 0, 1, 0, None) == -4                       # valid: no device here
