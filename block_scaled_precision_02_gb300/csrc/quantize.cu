@@ -50,14 +50,17 @@ namespace mxq {
 constexpr int TR = 128;                     // tile rows
 constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
 
-template <int NSTG, int NOUT, bool EXTRA>
+template <int NSTG, int NOUT, bool EXTRA, int SW = 8>
 struct TileCfg {
   static constexpr int TC = 64;                     // tile columns
   static constexpr int THREADS = 256;
   static constexpr int NW = THREADS / 32;
   static constexpr int IN_BYTES = TR * TC * 2;      // one stage: 128 x 64 bf16
   static constexpr int STG = 2048;                  // one staging buffer of one warp
-  static constexpr int SMEM = NSTG * IN_BYTES + NW * NOUT * STG + 256 + 1024;
+  // SW warps write codes: all eight, or the four column warps of a
+  // column-only launch (warps 0-3), whose smaller footprint fits a third CTA
+  static constexpr int SWARPS = SW;
+  static constexpr int SMEM = NSTG * IN_BYTES + SW * NOUT * STG + 256 + 1024;
   // resident CTAs per SM the registers are budgeted for
   static constexpr int MIN_BLOCKS = EXTRA ? 2 : (SMEM <= 70 * 1024 ? 3 : 2);
 };
@@ -342,9 +345,9 @@ __device__ __forceinline__ int job_of(const QuantLaunch<NJ>& L, int tile) {
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT, int NJ>
-__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA>::MIN_BLOCKS)
+__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams p0) {
-  using T = TileCfg<NSTG, NOUT, EXTRA>;
+  using T = TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8>;
   constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
@@ -361,8 +364,8 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* in_s = smem;                                   // NSTG x 16 KiB stages
-  uint8_t* stg_s = in_s + NSTG * T::IN_BYTES;             // per warp NOUT staging buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + T::NW * NOUT * T::STG);   // full[NSTG]
+  uint8_t* stg_s = in_s + NSTG * T::IN_BYTES;             // per code-writing warp NOUT staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + T::SWARPS * NOUT * T::STG);   // full[NSTG]
   uint32_t* cnt = reinterpret_cast<uint32_t*>(bars + NSTG);       // readers done with each stage
   int* last_use = reinterpret_cast<int*>(cnt + NSTG);             // latest load issued into each stage
   uint32_t* red = reinterpret_cast<uint32_t*>(last_use + NSTG);   // per-warp amax (per-tensor)
@@ -765,7 +768,7 @@ constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA, int NJ>
 int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
-  using T = TileCfg<QNST, QSTG, EXTRA>;
+  using T = TileCfg<QNST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8>;
   auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
