@@ -50,15 +50,18 @@ namespace mxq {
 constexpr int TR = 128;                     // tile rows
 constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
 
-template <int NSTG, int NOUT, bool EXTRA, int SW = 8>
+template <int NSTG, int NOUT, bool EXTRA, int SW = 8, int STG_ = 2048>
 struct TileCfg {
   static constexpr int TC = 64;                     // tile columns
   static constexpr int THREADS = 256;
   static constexpr int NW = THREADS / 32;
   static constexpr int IN_BYTES = TR * TC * 2;      // one stage: 128 x 64 bf16
-  static constexpr int STG = 2048;                  // one staging buffer of one warp
+  // one staging buffer of one warp: a dual launch's 32 rows (or 64 columns)
+  // of codes, 2 KiB; a row-only warp's 16 rows, 1 KiB
+  static constexpr int STG = STG_;
   // SW warps write codes: all eight, or the four column warps of a
-  // column-only launch (warps 0-3), whose smaller footprint fits a third CTA
+  // column-only launch (warps 0-3).  Column-only and row-only launches
+  // thereby need 65 KB of shared memory, which fits a third CTA per SM.
   static constexpr int SWARPS = SW;
   static constexpr int SMEM = NSTG * IN_BYTES + SW * NOUT * STG + 256 + 1024;
   // resident CTAs per SM the registers are budgeted for
@@ -345,9 +348,10 @@ __device__ __forceinline__ int job_of(const QuantLaunch<NJ>& L, int tile) {
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT, int NJ>
-__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8>::MIN_BLOCKS)
+__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8,
+                                               ORIENT == MXQ_ROW ? 1024 : 2048>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams p0) {
-  using T = TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8>;
+  using T = TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
   constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
@@ -359,7 +363,7 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
   constexpr int BPL = DUAL ? 2 : 1;                 // 1 x 32 blocks per lane of a row warp
   constexpr int ROW_WARPS = DO_ROW ? (DUAL ? 4 : 8) : 0;
   constexpr int ACTIVE = ROW_WARPS + (DO_COL ? 4 : 0);   // warps that read every stage
-  static_assert(RR * QBR <= T::STG && 64 * QBW <= T::STG, "staging buffer");
+  static_assert((!DO_ROW || RR * QBR <= T::STG) && (!DO_COL || 64 * QBW <= T::STG), "staging buffer");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -768,7 +772,7 @@ constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA, int NJ>
 int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
-  using T = TileCfg<QNST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8>;
+  using T = TileCfg<QNST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
   auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
