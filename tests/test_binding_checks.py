@@ -54,6 +54,20 @@ def test_dequantize_checks_scales_and_device():
         mxq.mx_dequantize(u8(64, 64), u8(64, 2), "e4m3", torch.int32)
 
 
+def test_quantize_group_checks_before_any_call():
+    x = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="between 1 and"):
+        mxq.mx_quantize_group([], "e4m3")
+    with pytest.raises(ValueError, match="between 1 and"):
+        mxq.mx_quantize_group([x] * 5, "e4m3")
+    with pytest.raises(ValueError, match="one scale mode"):
+        mxq.mx_quantize_group([x, x], "e4m3", "row", ["floor"])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mxq.mx_quantize_group([x], "e4m3")
+    with pytest.raises(KeyError):
+        mxq.mx_quantize_group([x], "e3m4")
+
+
 def test_mm_fp8_needs_byte_codes():
     a = torch.zeros(128, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="1-byte FP8 codes"):
