@@ -31,6 +31,9 @@
 //    Scales leave from the lanes that computed them, in the requested layout
 //    (canonical, or the GEMM's 512-byte tensor-core chunks).
 //  * One HBM read of x produces every requested output.
+//  * A launch may carry up to four tensors of one format and orientation
+//    (the grouped entry point): their tiles form one sequence, and each tile
+//    reads its own tensor's maps and parameters.
 #include <algorithm>
 
 #include "common.cuh"
