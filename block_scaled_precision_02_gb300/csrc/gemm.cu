@@ -451,7 +451,16 @@ __device__ __forceinline__ void store_row_scales(const Params& p, size_t rg, int
 // whole batched output) in the mode p.epi.  bf16 / float32 go through two
 // 64-byte-swizzled staging buffers and TMA stores issued by `leader`; all
 // 128 epilogue threads take part (named barrier 1).
-template <int BN, bool PER_TENSOR, int MXOUT, typename Release>
+// Before a staging buffer is rewritten: with two buffers the bulk store
+// issued from this one two chunks ago must have read it (at most one store
+// group still reading); with one buffer the last store must have.
+template <int NBUF>
+__device__ __forceinline__ void bulk_wait_read_staging() {
+  if constexpr (NBUF == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  else asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+template <int BN, bool PER_TENSOR, int MXOUT, int NBUF, typename Release>
 __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_t tmem, int q, int lane, bool leader,
                                            int& buf, uint8_t* sOut, const CUtensorMap* map_c, int m0, int n0,
                                            Release release) {
@@ -496,7 +505,7 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     release();
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
-      if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      if (leader) bulk_wait_read_staging<NBUF>();
       named_bar(1, 128);
       uint8_t* stg = sOut + buf * STG_BYTES;
 #pragma unroll
@@ -511,7 +520,7 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
         tma_store_2d(map_c, smem_u32(stg), n0 + c * 32, m0);
         bulk_commit();
       }
-      buf ^= 1;
+      buf ^= NBUF - 1;
     }
     return;
   }
@@ -652,7 +661,7 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
       release();
     }
     for (int h = 0; h < 2; ++h) {
-      if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      if (leader) bulk_wait_read_staging<NBUF>();
       named_bar(1, 128);
       uint8_t* stg = sOut + buf * STG_BYTES;
 #pragma unroll
@@ -667,7 +676,7 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
         tma_store_2d(map_c, smem_u32(stg), n0 + c0 + h * 16, m0);
         bulk_commit();
       }
-      buf ^= 1;
+      buf ^= NBUF - 1;
     }
   }
 }
@@ -945,7 +954,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       named_bar(1, 128);
       if (*epi_fail) { *abort_flag = 1; break; }
       tc_fence_after();
-      store_tile<BN, C::KIND == KIND_F8, MXOUT>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, tp.b * p.M + tp.m0,
+      store_tile<BN, C::KIND == KIND_F8, MXOUT, 2>(p, alpha, tmem, q, lane, leader, buf, sOut, &map_c, tp.b * p.M + tp.m0,
                                          tp.n0, [&] {
                                            if (lane == 0) mbar_arrive(smem_u32(acc_empty));
                                          });
@@ -975,7 +984,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // sub-partition that work is latency-bound, so these variants run two groups
 // of four epilogue warps (warps 2-5 and 7-10), each draining 128 of the 256
 // accumulator columns.
-template <int KIND_, int MXOUT_ = 0>
+template <int KIND_, int MXOUT_ = 0, bool SK_ = false>
 struct PairCfg {
   static constexpr int KIND = KIND_;
   static constexpr bool FP4 = KIND == KIND_MXF4;
@@ -986,8 +995,13 @@ struct PairCfg {
   static constexpr int THREADS = PAIR_THREADS + (EPI_GROUPS - 1) * 128;
   // the column-block output transposes through 32 x 33 words per epilogue warp
   static constexpr bool MX_COLS = MXOUT_ == 2 || MXOUT_ == 4;     // MX column blocks too
-  static constexpr int OUT = MX_COLS ? EPI_GROUPS * XS_GROUP_BYTES : OUT_BYTES;
-  static constexpr int STAGES = (FP4 || MX_COLS) ? 5 : 6;
+  // MXFP4 with bf16 / float32 output: one staging buffer (the epilogue runs
+  // after the accumulator is released, off the MMAs' path), which leaves
+  // room for a sixth stage
+  static constexpr bool ONE_STG = FP4 && MXOUT_ == 0 && !SK_;
+  static constexpr int NBUF = ONE_STG ? 1 : 2;
+  static constexpr int OUT = MX_COLS ? EPI_GROUPS * XS_GROUP_BYTES : (ONE_STG ? STG_BYTES + 512 : OUT_BYTES);
+  static constexpr int STAGES = ONE_STG ? 6 : ((FP4 || MX_COLS) ? 5 : 6);
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
   static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
@@ -1007,11 +1021,11 @@ struct PairCfg {
 };
 
 template <int KIND, int MXOUT, bool SK = false>
-__global__ void __launch_bounds__(PairCfg<KIND, MXOUT>::THREADS, 1)
+__global__ void __launch_bounds__(PairCfg<KIND, MXOUT, SK>::THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
                     const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using C = PairCfg<KIND, MXOUT>;
+  using C = PairCfg<KIND, MXOUT, SK>;
   constexpr int STAGES_P = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1257,7 +1271,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           continue;
         }
       }
-      store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT>(
+      store_tile<C::EPI_COLS, C::KIND == KIND_F8, MXOUT, C::NBUF>(
           p, alpha, tmem + ab * C::BN + grp * C::EPI_COLS, q, lane, leader, buf, sOut + grp * XS_GROUP_BYTES,
           &map_c, m0, tp.n0 + grp * C::EPI_COLS, release);
     }
@@ -1516,15 +1530,16 @@ int launch_pair(const GemmArgs& g, int pairs, cudaStream_t st) {
     const int last = p.ntiles % pairs;                     // tiles in the last, partial wave
     const bool worth = p.ntiles > pairs && last > 0 && last <= kSkMaxLastWave * pairs;
     if (g.ws && worth) {
+      using Ck = PairCfg<KIND, MXOUT, true>;
       auto kern = mx_gemm_pair_kernel<KIND, MXOUT, true>;
-      const int sk_pairs = max_pairs<KIND, MXOUT, true>(kern, Cf::SMEM, Cf::THREADS);
+      const int sk_pairs = max_pairs<KIND, MXOUT, true>(kern, Ck::SMEM, Ck::THREADS);
       if (sk_pairs == pairs && g.ws_bytes >= sk_workspace_bytes(pairs)) {
         p.sk = 1;
         p.sk_dp = (p.ntiles / pairs - 1) * pairs;
         p.sk_flags = static_cast<uint32_t*>(g.ws);
         p.sk_part = reinterpret_cast<float*>(static_cast<uint8_t*>(g.ws) + sk_flag_bytes(pairs));
         p.sk_epoch = next_epoch();
-        return launch_pdl_cluster(kern, dim3(2 * pairs), dim3(Cf::THREADS), Cf::SMEM, st, 2, ma, mb, msa, msb, mc,
+        return launch_pdl_cluster(kern, dim3(2 * pairs), dim3(Ck::THREADS), Ck::SMEM, st, 2, ma, mb, msa, msb, mc,
                                   p);
       }
     }
