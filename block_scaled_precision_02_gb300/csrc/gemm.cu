@@ -1000,8 +1000,11 @@ struct PairCfg {
   // room for a sixth stage
   static constexpr bool ONE_STG = FP4 && MXOUT_ == 0 && !SK_;
   static constexpr int NBUF = ONE_STG ? 1 : 2;
-  static constexpr int OUT = MX_COLS ? EPI_GROUPS * XS_GROUP_BYTES : (ONE_STG ? STG_BYTES + 512 : OUT_BYTES);
-  static constexpr int STAGES = ONE_STG ? 6 : ((FP4 || MX_COLS) ? 5 : 6);
+  // MX row blocks alone are stored straight from registers: no staging
+  static constexpr bool MX_ROWS_ONLY = MXOUT_ == 1 || MXOUT_ == 3;
+  static constexpr int OUT =
+      MX_COLS ? EPI_GROUPS * XS_GROUP_BYTES : (MX_ROWS_ONLY ? 0 : (ONE_STG ? STG_BYTES + 512 : OUT_BYTES));
+  static constexpr int STAGES = (ONE_STG || (FP4 && MX_ROWS_ONLY)) ? 6 : ((FP4 || MX_COLS) ? 5 : 6);
   static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKB;        // this CTA's 128 rows of B
   static constexpr int SF_CHUNKS = SCALED ? (FP4 ? 2 : 1) : 0;   // 512-B chunks per 128 rows per stage
