@@ -186,6 +186,22 @@ def test_pm_one_operands_integer_sums(lib):
     assert np.array_equal(got, a @ b.T)
 
 
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_fp4_many_tiles_exact(lib, out):
+    """MXFP4 with bf16 and float32 output over 256 pair tiles (several per
+    CTA pair, so the epilogue's one staging buffer is reused across tiles
+    and chunks): +-1 operands give even integer sums of magnitude at most
+    512, exact in float32 and in bf16, so C equals a @ b^T exactly."""
+    rng = np.random.default_rng(12)
+    M, N, K = 4096, 4096, 512
+    a = rng.choice([-1.0, 1.0], (M, K))
+    b = rng.choice([-1.0, 1.0], (N, K))
+    aq, as_ = oracle_operand(a, "e2m1")
+    bq, bs = oracle_operand(b, "e2m1")
+    got = gpu_gemm(lib, aq, as_, bq, bs, "e2m1", out)
+    assert np.array_equal(got, a @ b.T)
+
+
 def _sampled(lib, M, N, K, fmt, gen_a, gen_b, nrows=64, ncols=64):
     a = f64(gen_a(M, K))
     b = f64(gen_b(N, K))
