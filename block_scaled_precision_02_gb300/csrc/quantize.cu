@@ -771,12 +771,17 @@ namespace {
 
 constexpr int QTC = TileCfg<1, 1, false>::TC;
 constexpr int QNST = MXQ_QUANT_NST;
+// The stochastic-rounding / Hadamard variants are bound by their arithmetic;
+// two stages serve them better than three (measured: SR, SR4 and the
+// Hadamard RNE quantize of 4096 x 14336 about 3-5 % faster).
+constexpr int QNST_EXTRA = 2;
 constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA, int NJ>
 int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
-  using T = TileCfg<QNST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
-  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, QNST, QSTG, NJ>;
+  constexpr int NST = EXTRA ? QNST_EXTRA : QNST;
+  using T = TileCfg<NST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
+  auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, NST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
   static int per_sm[64] = {};
