@@ -186,3 +186,23 @@ def test_group_argument_checks_need_no_gpu(so):
     bad = (QuantJob * 1)(QuantJob(0x10000, 64, 64, 64, 0, 0x10000, 0x10000, 0, 0))
     assert g(bad, 1, 0, 3, 0, None) == -1                        # DUAL without column outputs
     assert g(jobs, 4, 0, 1, 0, None) == -4                       # valid: no device here
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/mxq.h is a C header: a C99 translation unit that uses its
+    types and constants compiles (no C++ or torch types leak into it)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "mxq.h"\n'
+                   "int main(void) {\n"
+                   "  mxq_quant_job j = {0};\n"
+                   "  (void)j;\n"
+                   "  return MXQ_QUANT_GROUP_MAX + MXQ_E2M1 + MXQ_SF_MMA;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
