@@ -20,6 +20,8 @@ measured on):
 * ``heavy_gradient``  4096 x 14336, 1e-2 * t_3 / sqrt(3) (Student-t, nu = 3,
   normalised to variance 1e-4).  Seed 6.
 * ``fp4_operand``     4096 x 14336, N(0, 1).  Seed 8.
+* ``tiled_large``     beyond 2^31 elements: tiles of a seeded block, each
+  scaled by 2^e, e ~ U{-3..3} (seed 9), for the 64-bit indexing cases.
 """
 
 from __future__ import annotations
@@ -102,6 +104,39 @@ def heavy_gradient(rows: int = 4096, cols: int = 14336, seed: int = 6) -> torch.
 
 def fp4_operand(rows: int = 4096, cols: int = 14336, seed: int = 8) -> torch.Tensor:
     return normal(rows, cols, 1.0, seed)
+
+
+def tiled_large(rows: int, cols: int, block: torch.Tensor, seed: int = 9) -> torch.Tensor:
+    """A tensor larger than 2^31 elements built on ``block``'s device from a
+    small block: tile (i, j) of the result is ``block * 2^e_ij`` with e_ij ~
+    U{-3..3} (seed ``seed``; a power of two keeps every bf16 value exact),
+    so neighbouring tiles differ in scale.  ``tiled_large_rows`` rebuilds
+    any rows of it on the CPU."""
+    br, bc = block.shape
+    e = tiled_large_exponents(rows // br, cols // bc, seed)
+    f = torch.from_numpy(np.exp2(e).astype(np.float32)).to(block.device)
+    out = torch.empty(rows, cols, dtype=torch.bfloat16, device=block.device)
+    for i in range(rows // br):
+        for j in range(cols // bc):
+            out[i * br:(i + 1) * br, j * bc:(j + 1) * bc] = (block.float() * f[i, j]).to(torch.bfloat16)
+    return out
+
+
+def tiled_large_exponents(ti: int, tj: int, seed: int = 9) -> np.ndarray:
+    return np.random.default_rng(seed).integers(-3, 4, size=(ti, tj)).astype(np.float64)
+
+
+def tiled_large_rows(rows_idx, cols: int, block: torch.Tensor, nrows: int, seed: int = 9) -> torch.Tensor:
+    """Rows ``rows_idx`` of ``tiled_large(nrows, cols, block, seed)``, on the CPU."""
+    br, bc = block.shape
+    e = tiled_large_exponents(nrows // br, cols // bc, seed)
+    b = block.cpu().float()
+    rows = []
+    for r in rows_idx:
+        i = r // br
+        f = torch.from_numpy(np.repeat(np.exp2(e[i]).astype(np.float32), bc))
+        rows.append((b[r % br].repeat(cols // bc) * f).to(torch.bfloat16))
+    return torch.stack(rows)
 
 
 def special_values_bf16() -> np.ndarray:
