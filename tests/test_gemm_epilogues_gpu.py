@@ -454,10 +454,12 @@ def test_full_size_mxfp4_e2m1_output_sampled(lib):
     assert np.mean(F.unpack_fp4(cq[rows]) == F.unpack_fp4(want["q_row"])) >= 0.99
 
 
-def test_full_size_mm_fp8_sampled(lib):
-    """The bench's per-tensor FP8 product at full size and launch
-    configuration: 8192 x 4096 E4M3 operand times the transposed view of a
-    4096 x 4096 one, with bias; sampled rows and columns within the gate."""
+@pytest.mark.parametrize("kn", [False, True])
+def test_full_size_mm_fp8_sampled(lib, kn):
+    """The bench's per-tensor FP8 products at full size and launch
+    configuration: 8192 x 4096 E4M3 operand times a 4096 x 4096 weight with
+    bias, the weight stored [N][K] (transposed view) or [K][N] (the default
+    layout, read N-contiguous); sampled rows and columns within the gate."""
     M, N, K = 8192, 4096, 4096
     rng = np.random.default_rng(27)
     # seeded finite E4M3 codes (every code but the NaN patterns 0x7F / 0xFF)
@@ -465,7 +467,10 @@ def test_full_size_mm_fp8_sampled(lib):
     w8n = (rng.integers(0, 0x7F, (N, K), dtype=np.uint8) | (rng.integers(0, 2, (N, K), dtype=np.uint8) << 7))
     bias = inputs.weights(1, N, seed=9).reshape(N)
     sc = torch.tensor([0.75], dtype=torch.float32, device=dev)
-    c = lib.mm_fp8(t(x8n), t(w8n), sc, trans_b=True, bias=bias.to(dev), fmt="e4m3").float().cpu().numpy()
+    if kn:
+        c = lib.mm_fp8(t(x8n), t(w8n.T), sc, bias=bias.to(dev), fmt="e4m3").float().cpu().numpy()
+    else:
+        c = lib.mm_fp8(t(x8n), t(w8n), sc, trans_b=True, bias=bias.to(dev), fmt="e4m3").float().cpu().numpy()
     rows, cols = _rows(M, 64, 4), _rows(N, 64, 5)
     ref = og.mm_fp8_reference(x8n[rows], w8n[cols], F.E4M3, 0.75, f64(bias)[cols])
     assert og.gate_error(c[np.ix_(rows, cols)].astype(np.float64), ref) <= 2e-3

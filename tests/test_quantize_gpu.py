@@ -408,5 +408,32 @@ def test_full_size_pertensor_sixteen_steps(lib):
         assert_bytes_equal(np_(ring).view(np.uint32), ring_ref.view(np.uint32), f"ring step {t}")
 
 
+def test_full_size_pertensor_transposed_sixteen_steps(lib):
+    """The benchmark's transposed-only per-tensor row: 4096 x 14336, 16
+    steps of ``quantize(x_t, scale, transposed=True, ring)`` (x8T only),
+    each with the multiplier the previous fold published.  Each step:
+    sampled columns of x (rows of x8T) against the oracle, and every ring
+    slot equal to the oracle's host fold."""
+    dev = torch.device("cuda")
+    base = inputs.pertensor_base()
+    bv = f64(base)
+    amax0 = float(np.max(np.abs(bv)))
+    exps = inputs.pertensor_step_exponents(16, seed=3)
+    base_d = base.to(dev)
+    n = 16
+    ring = lib.ring_state_new(n, dev)
+    ring_ref = opt.ring_new(n)
+    cols = _sample_rows(14336, 8, 8)
+    for t, v in enumerate(exps):
+        xt = inputs.pertensor_step(base_d, v)
+        m = float(ring_ref[n + 1])
+        x8T, _ = lib.quantize(xt, ring[n + 1:n + 2], "e4m3", True, ring, t % n)
+        assert x8T.shape == (14336, 4096)
+        r8, _, _ = opt.quantize_pertensor(bv[:, cols].T * 2.0 ** v, m, F.E4M3)
+        ring_ref = opt.ring_fold(ring_ref, amax0 * 2.0 ** v, t % n)
+        assert_bytes_equal(np_(x8T)[cols], r8, f"x8T sample, step {t}")
+        assert_bytes_equal(np_(ring).view(np.uint32), ring_ref.view(np.uint32), f"ring step {t}")
+
+
 def test_device_status_clean(lib):
     assert lib.last_device_status() == 0
