@@ -97,6 +97,35 @@ def test_stream_k_gate_and_agreement(lib, fa, fb, K, waves):
     assert np.array_equal(run(lib, aq, as_, bq, bs, fa, fb, True, torch.float32), sk32)
 
 
+def test_full_size_sparse_tail_sampled(lib):
+    """The bench's sparse-tail product at full size: 2560 x 2048 x 16384
+    MXFP8 (80 tiles on the CTA pairs), stream-K and plain schedules.
+    Sampled rows and columns within the gate, and the two schedules'
+    float32 outputs within a few float32 roundings of each other."""
+    M, N, K = 2560, 2048, 16384
+    a = f64(inputs.activations(M, K, seed=0))
+    b = f64(inputs.weights(N, K, seed=4))
+    aq, as_ = operand(a, "e4m3")
+    bq, bs = operand(b, "e4m3")
+    sk = run(lib, aq, as_, bq, bs, "e4m3", "e4m3", True)
+    plain = run(lib, aq, as_, bq, bs, "e4m3", "e4m3", False)
+    rng = np.random.default_rng(11)
+    rows = np.sort(rng.choice(M, 48, replace=False))
+    cols = np.sort(rng.choice(N, 48, replace=False))
+    ref = og.reference_rows_cols(aq, as_, bq, bs, F.E4M3, rows, cols)
+    assert og.gate_error(sk[np.ix_(rows, cols)], ref) <= 2e-3
+    assert og.gate_error(plain[np.ix_(rows, cols)], ref) <= 2e-3
+    # Both schedules add K/32 float32 MMA partial sums; splitting the
+    # running sum in two changes at most a few roundings per step, each at
+    # most 2^-24 of the running sum's size (bounded by the scale below).
+    # With K = 16384 that is a looser bound than the 1e-5 of the short-K
+    # shapes above.
+    sk32 = run(lib, aq, as_, bq, bs, "e4m3", "e4m3", True, torch.float32)
+    plain32 = run(lib, aq, as_, bq, bs, "e4m3", "e4m3", False, torch.float32)
+    scale = np.maximum(np.abs(plain32), np.sqrt(np.mean(plain32 ** 2)))
+    assert np.max(np.abs(sk32 - plain32) / scale) <= 2 * 2.0 ** -24 * (K // 32)
+
+
 def test_stream_k_without_workspace_is_the_plain_schedule(lib):
     M, N = shape_with_tail(1)
     K = 256
