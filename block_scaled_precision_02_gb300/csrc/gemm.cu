@@ -42,7 +42,7 @@
 //  * warps 2..5  epilogue: tcgen05.ld of this CTA's 128 x N float32
 //                accumulator rows (each thread owns one row), conversion,
 //                and stores (TMA through two 64-byte-swizzled staging
-//                buffers; the MX output is stored directly).  The pair
+//                buffers, one for MXFP4; the MX output is stored directly).  The pair
 //                kernel's MX-output variants add warps 7..10, a second
 //                epilogue group that takes the other half of the columns,
 //                and read all of a group's columns into registers before
@@ -448,8 +448,8 @@ __device__ __forceinline__ void store_row_scales(const Params& p, size_t rg, int
 // accumulator (tensor-memory lanes 0..127, columns 0..BN-1; the thread of
 // lane quarter q and lane `lane` owns row 32 q + lane), call release() once
 // it has been read completely, and store it to C[m0 .., n0 ..] (rows of the
-// whole batched output) in the mode p.epi.  bf16 / float32 go through two
-// 64-byte-swizzled staging buffers and TMA stores issued by `leader`; all
+// whole batched output) in the mode p.epi.  bf16 / float32 go through NBUF
+// (two, or one) 64-byte-swizzled staging buffers and TMA stores issued by `leader`; all
 // 128 epilogue threads take part (named barrier 1).
 // Before a staging buffer is rewritten: with two buffers the bulk store
 // issued from this one two chunks ago must have read it (at most one store
@@ -603,8 +603,9 @@ __device__ __forceinline__ void store_tile(const Params& p, float alpha, uint32_
     // from the registers and stored at once (only the scale words are kept
     // to the end).  Column blocks: a warp's 32 rows of a chunk are 32 blocks
     // of 32 x 1; the warp transposes the chunk through its part of the (here
-    // unused) staging area, rows padded to 33 words so that neither the row
-    // writes nor the column reads conflict, and lane j quantizes column j.
+    // unused) staging area, rows XS_PITCH words apart so that neither the
+    // 16-byte row writes nor the column reads conflict, and lane j quantizes
+    // column j.
     uint32_t sc[BN / 128];
     uint32_t* xs = reinterpret_cast<uint32_t*>(sOut) + q * XS_WORDS;    // this warp's transpose scratch
     const size_t rg = static_cast<size_t>(m0 + row);
