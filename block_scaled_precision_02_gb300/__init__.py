@@ -28,11 +28,25 @@ FLOOR_OCP, CEIL = 0, 1
 RNE, SR, SR4 = 0, 1, 2
 SF_CANONICAL, SF_MMA = 0, 1
 
-_FMT = {"e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1, E4M3: E4M3, E5M2: E5M2, E2M1: E2M1}
-_ORIENT = {"row": ROW, "col": COL, "dual": DUAL, ROW: ROW, COL: COL, DUAL: DUAL}
-_SCALE = {"floor": FLOOR_OCP, "floor_ocp": FLOOR_OCP, "ceil": CEIL, FLOOR_OCP: FLOOR_OCP, CEIL: CEIL}
-_ROUND = {"rne": RNE, "sr": SR, "stochastic": SR, "sr4": SR4, RNE: RNE, SR: SR, SR4: SR4}
-_SF = {"canonical": SF_CANONICAL, "mma": SF_MMA, SF_CANONICAL: SF_CANONICAL, SF_MMA: SF_MMA}
+class _Choices(dict):
+    """Name (or code) -> library code; an unknown name is a ValueError."""
+
+    def __init__(self, what: str, items: dict):
+        super().__init__(items)
+        self.what = what
+
+    def __missing__(self, key):
+        names = sorted(k for k in self if isinstance(k, str))
+        raise ValueError(f"unknown {self.what} {key!r} (one of {', '.join(names)})")
+
+
+_FMT = _Choices("format", {"e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1, E4M3: E4M3, E5M2: E5M2, E2M1: E2M1})
+_ORIENT = _Choices("orientation", {"row": ROW, "col": COL, "dual": DUAL, ROW: ROW, COL: COL, DUAL: DUAL})
+_SCALE = _Choices("scale mode", {"floor": FLOOR_OCP, "floor_ocp": FLOOR_OCP, "ceil": CEIL, FLOOR_OCP: FLOOR_OCP,
+                                 CEIL: CEIL})
+_ROUND = _Choices("rounding", {"rne": RNE, "sr": SR, "stochastic": SR, "sr4": SR4, RNE: RNE, SR: SR, SR4: SR4})
+_SF = _Choices("scale layout", {"canonical": SF_CANONICAL, "mma": SF_MMA, SF_CANONICAL: SF_CANONICAL,
+                                SF_MMA: SF_MMA})
 
 _lib = None
 
@@ -213,11 +227,12 @@ def mx_quantize_group(xs, fmt="e4m3", orientation="row", scale_modes="floor", sf
     modes = [scale_modes] * len(xs) if isinstance(scale_modes, str) else list(scale_modes)
     if len(modes) != len(xs):
         raise ValueError("one scale mode, or one per tensor")
-    f, o = _FMT[fmt], _ORIENT[orientation]
+    f, o, sf = _FMT[fmt], _ORIENT[orientation], _SF[sf_layout]
+    codes = [_SCALE[m] for m in modes]
     qb = 2 if f == E2M1 else 1
     dev = None
     outs, jobs = [], (QuantJob * len(xs))()
-    for k, (x, mode) in enumerate(zip(xs, modes)):
+    for k, (x, mode) in enumerate(zip(xs, codes)):
         _cuda_2d(x, f"xs[{k}]")
         if x.dtype != torch.bfloat16 or x.stride(1) != 1:
             raise ValueError("every tensor must be bf16 with a contiguous last dimension")
@@ -231,10 +246,10 @@ def mx_quantize_group(xs, fmt="e4m3", orientation="row", scale_modes="floor", sf
         if o & COL:
             q_col = torch.empty(cols, rows // qb, dtype=torch.uint8, device=dev)
             s_col = torch.empty(cols, rows // 32, dtype=torch.uint8, device=dev)
-        jobs[k] = QuantJob(x.data_ptr(), rows, cols, x.stride(0), _SCALE[mode],
+        jobs[k] = QuantJob(x.data_ptr(), rows, cols, x.stride(0), mode,
                            *[0 if t is None else t.data_ptr() for t in (q_row, s_row, q_col, s_col)])
         outs.append((q_row, s_row, q_col, s_col))
-    _call("mxq_quantize_group", dev, jobs, len(xs), f, o, _SF[sf_layout])
+    _call("mxq_quantize_group", dev, jobs, len(xs), f, o, sf)
     return outs
 
 

@@ -64,8 +64,10 @@ def test_quantize_group_checks_before_any_call():
         mxq.mx_quantize_group([x, x], "e4m3", "row", ["floor"])
     with pytest.raises(ValueError, match="CUDA tensor"):
         mxq.mx_quantize_group([x], "e4m3")
-    with pytest.raises(KeyError):
+    with pytest.raises(ValueError, match="unknown format 'e3m4'"):
         mxq.mx_quantize_group([x], "e3m4")
+    with pytest.raises(ValueError, match="unknown scale mode"):
+        mxq.mx_quantize_group([x], "e4m3", "row", "round")
 
 
 def test_mm_fp8_needs_byte_codes():
