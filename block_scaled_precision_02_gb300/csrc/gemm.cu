@@ -355,48 +355,111 @@ __device__ __forceinline__ uint32_t mma_idesc(const Params& p, int n, int m, int
   else return instr_desc(p.a_type, p.b_type, n, m, KIND == KIND_MXF4 ? (kk & 1) * 2 : kk);
 }
 
-// Four float32 -> four FP8 codes (RNE, saturating) in the given format.
-__device__ __forceinline__ uint32_t fp8x4_rt(int fmt, float a, float b, float c, float d) {
-  return fmt == MXQ_E4M3 ? cvt_fp8x4<MXQ_E4M3>(a, b, c, d) : cvt_fp8x4<MXQ_E5M2>(a, b, c, d);
+// NaN-propagating maxima of two or three float32 values (a NaN operand
+// gives NaN; no flush of subnormals).
+__device__ __forceinline__ float fmax2n(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3n(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Bits of the largest magnitude among 32 float32 words, by a tree of
+// three-input maxima over the absolute values: a NaN anywhere gives NaN
+// bits, an infinity 0x7F800000, otherwise the largest |v| exactly -- the same
+// as the unsigned maximum of the sign-cleared bits.
+__device__ __forceinline__ uint32_t amax32_bits(const uint32_t (&v)[32]) {
+  auto a = [&](int j) { return fabsf(__uint_as_float(v[j])); };
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = fmax3n(a(3 * i), a(3 * i + 1), a(3 * i + 2));
+  t[10] = fmax2n(a(30), a(31));
+  const float u = fmax3n(fmax3n(t[0], t[1], t[2]), fmax3n(t[3], t[4], t[5]), fmax3n(t[6], t[7], t[8]));
+  return __float_as_uint(fmax3n(u, t[9], t[10])) & 0x7FFFFFFFu;
+}
+
+// FP8 codes of four float32 words each multiplied by m (mm = m twice; one
+// packed multiply per pair, rounded to nearest like the scalar product),
+// converted RNE-saturating; the first word's code in the lowest byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x4_scaled(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint64_t mm) {
+  uint32_t r;
+  if constexpr (FMT == MXQ_E4M3) {
+    asm("{\n\t.reg .b64 pa, pb;\n\t.reg .b32 a0, a1, b0, b1;\n\t.reg .b16 t0, t1;\n\t"
+        "mov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %4};\n\t"
+        "mul.rn.f32x2 pa, pa, %5;\n\tmul.rn.f32x2 pb, pb, %5;\n\t"
+        "mov.b64 {a0, a1}, pa;\n\tmov.b64 {b0, b1}, pb;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t0, a1, a0;\n\tcvt.rn.satfinite.e4m3x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "r"(a), "r"(b), "r"(c), "r"(d), "l"(mm));
+  } else {
+    asm("{\n\t.reg .b64 pa, pb;\n\t.reg .b32 a0, a1, b0, b1;\n\t.reg .b16 t0, t1;\n\t"
+        "mov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %4};\n\t"
+        "mul.rn.f32x2 pa, pa, %5;\n\tmul.rn.f32x2 pb, pb, %5;\n\t"
+        "mov.b64 {a0, a1}, pa;\n\tmov.b64 {b0, b1}, pb;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 t0, a1, a0;\n\tcvt.rn.satfinite.e5m2x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r) : "r"(a), "r"(b), "r"(c), "r"(d), "l"(mm));
+  }
+  return r;
+}
+
+// E2M1 codes of eight float32 words each multiplied by m (packed multiplies
+// as above), RNE-saturating, packed two per byte: the first word's code in
+// the lowest nibble.
+__device__ __forceinline__ uint32_t e2m1x8_scaled(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                                  uint32_t f, uint32_t g, uint32_t h, uint64_t mm) {
+  uint32_t r;
+  asm("{\n\t.reg .b64 p0, p1, p2, p3;\n\t.reg .b32 x<8>;\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "mov.b64 p0, {%1, %2};\n\tmov.b64 p1, {%3, %4};\n\tmov.b64 p2, {%5, %6};\n\tmov.b64 p3, {%7, %8};\n\t"
+      "mul.rn.f32x2 p0, p0, %9;\n\tmul.rn.f32x2 p1, p1, %9;\n\t"
+      "mul.rn.f32x2 p2, p2, %9;\n\tmul.rn.f32x2 p3, p3, %9;\n\t"
+      "mov.b64 {x0, x1}, p0;\n\tmov.b64 {x2, x3}, p1;\n\tmov.b64 {x4, x5}, p2;\n\tmov.b64 {x6, x7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, x1, x0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, x3, x2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, x5, x4;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, x7, x6;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r) : "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h), "l"(mm));
+  return r;
 }
 
 // MX quantization of one 32-value row block of the accumulator: the scale
 // rule of the quantizer (floor or ceil on the block amax's exponent and
 // mantissa bits), then codes = RNE-saturating FP8 of v * 2^-e (exact
 // product).  A block holding NaN or Inf gets scale 0xFF and zero codes.
-__device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt, int ceil_mode,
-                                               uint32_t* codes /* 8 words */) {
-  uint32_t ab = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) ab = max(ab, v[j] & 0x7FFFFFFFu);
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_block32_fmt(const uint32_t (&v)[32], int ceil_mode, uint32_t* codes) {
+  const uint32_t ab = amax32_bits(v);
   const bool bad = ab >= 0x7F800000u;
-  const int e = bad ? 0 : (fmt == MXQ_E4M3 ? scale_exp<MXQ_E4M3>(ab, ceil_mode) : scale_exp<MXQ_E5M2>(ab, ceil_mode));
-  const float m = exp2_neg(e);
+  const int e = bad ? 0 : scale_exp<FMT>(ab, ceil_mode);
+  const uint64_t mm = f32x2_splat(exp2_neg(e));
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t x = fp8x4_rt(fmt, __fmul_rn(__uint_as_float(v[4 * k]), m), __fmul_rn(__uint_as_float(v[4 * k + 1]), m),
-                                __fmul_rn(__uint_as_float(v[4 * k + 2]), m), __fmul_rn(__uint_as_float(v[4 * k + 3]), m));
+    const uint32_t x = fp8x4_scaled<FMT>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], mm);
     codes[k] = bad ? 0u : x;
   }
   return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
+}
+__device__ __forceinline__ uint32_t mx_block32(const uint32_t (&v)[32], int fmt, int ceil_mode,
+                                               uint32_t* codes /* 8 words */) {
+  return fmt == MXQ_E4M3 ? mx_block32_fmt<MXQ_E4M3>(v, ceil_mode, codes)
+                         : mx_block32_fmt<MXQ_E5M2>(v, ceil_mode, codes);
 }
 
 // The same for E2M1 output: codes in 4 words, eight nibbles each (element 0
 // in the lowest nibble).
 __device__ __forceinline__ uint32_t mx_block32_e2m1(const uint32_t (&v)[32], int ceil_mode, uint32_t* codes /* 4 words */) {
-  uint32_t ab = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) ab = max(ab, v[j] & 0x7FFFFFFFu);
+  const uint32_t ab = amax32_bits(v);
   const bool bad = ab >= 0x7F800000u;
   const int e = bad ? 0 : scale_exp<MXQ_E2M1>(ab, ceil_mode);
-  const float m = exp2_neg(e);
+  const uint64_t mm = f32x2_splat(exp2_neg(e));
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint32_t x = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      x |= cvt_e2m1x2(__fmul_rn(__uint_as_float(v[8 * k + 2 * j]), m), __fmul_rn(__uint_as_float(v[8 * k + 2 * j + 1]), m))
-           << (8 * j);
+    const uint32_t x = e2m1x8_scaled(v[8 * k], v[8 * k + 1], v[8 * k + 2], v[8 * k + 3], v[8 * k + 4], v[8 * k + 5],
+                                     v[8 * k + 6], v[8 * k + 7], mm);
     codes[k] = bad ? 0u : x;
   }
   return bad ? 0xFFu : static_cast<uint32_t>(e + 127);
