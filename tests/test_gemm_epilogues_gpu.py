@@ -88,6 +88,47 @@ def test_mx_output_exact_on_integer_products(lib, out_fmt, mode, layout, mnk, or
         assert cqT is None
 
 
+@pytest.mark.parametrize("out_fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+@pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 256)])
+def test_mx_output_nonfinite_blocks(lib, out_fmt, layout, mnk):
+    """Accumulator rows that are not finite: row m0 takes a NaN scale (UE8M0
+    0xFF) on its first k-block, row m1 the scale 2^127, which drives every
+    product of that k-block past float32's range (the first k-block's A and
+    B values are all positive, so no cancellation can bring the sum back).
+    Every 1x32 row block of those rows and every 32x1 column block of their
+    32-row bands must carry scale 0xFF and zero codes; all other blocks are
+    the oracle's quantization of the exact integer product.  The float32
+    overflow is written into the float64 reference by hand (the oracle's sum
+    is finite in float64)."""
+    M, N, K = mnk
+    rng = np.random.default_rng(33)
+    a = rng.choice([-1.0, 1.0], (M, K)) * np.exp2(rng.integers(-8, 9, size=(M, 1)))
+    a[:, :32] = np.abs(a[:, :32])
+    b = rng.integers(-4, 5, (N, K)).astype(np.float64)
+    b[:, :32] = rng.integers(1, 5, (N, 32))
+    aq, as_ = mx_operand(a, "e4m3")
+    bq, bs = mx_operand(b, "e4m3")
+    m0, m1 = 5, M - 40
+    as_ = as_.copy()
+    as_[m0, 0] = 0xFF
+    as_[m1, 0] = 0xFE
+    ref = og.reference(aq, as_, bq, bs, F.E4M3)
+    assert np.isnan(ref[m0]).all() and np.isfinite(np.delete(ref, [m0], axis=0)).all()
+    assert (np.abs(ref[m1]) > 2.0 ** 128).all()
+    ref[m1] = np.inf
+    want = omx.quantize(ref, FMTS[out_fmt], omx.DUAL, omx.FLOOR)
+    cq, cs, cqT, csT = run_mx_out(lib, aq, as_, bq, bs, "e4m3", out_fmt, "floor", layout, "dual")
+    for m in (m0, m1):
+        assert (cs[m] == 0xFF).all() and (want["s_row"][m] == 0xFF).all()
+        assert (cq[m] == 0).all()
+        assert (csT[:, m // 32] == 0xFF).all() and (want["s_col"][:, m // 32] == 0xFF).all()
+    assert_bytes_equal(cq, want["q_row"], "codes")
+    assert_bytes_equal(cs, want["s_row"], "scales")
+    assert_bytes_equal(cqT, want["q_col"], "column-block codes")
+    assert_bytes_equal(csT, want["s_col"], "column-block scales")
+
+
 @pytest.mark.parametrize("fa,fb", [("e4m3", "e2m1"), ("e2m1", "e4m3")])
 @pytest.mark.parametrize("mnk", [(128, 256, 512), (256, 512, 384)])
 def test_mx_output_exact_fp8_x_fp4(lib, fa, fb, mnk):
