@@ -133,29 +133,79 @@ __device__ __forceinline__ uint32_t sr_draw4(uint64_t idx, uint32_t k0, uint32_t
 
 constexpr float kHadC = 0.17677669529663688f;  // float32 nearest 1/sqrt(32)
 
+// Packed pairs of float32 (first element in the low half) and the packed
+// operations on them: each half rounds to nearest exactly as the scalar
+// operation would.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Fixed-sign 32-point Hadamard of one block held by one thread:
 // u_j = s_j v_j; butterflies h = 1, 2, 4, 8, 16 in that order,
 // (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h}) for (i & h) == 0;
 // y_j = RN32(u_j * c).  Every operation is a separate float32 rounding.
+// From h = 2 on, elements 2k and 2k + 1 meet elements 2k + h and
+// 2k + 1 + h, so those stages and the final product run on packed pairs.
 __device__ __forceinline__ void hadamard32(float (&u)[32], uint32_t signs) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) u[j] = ((signs >> j) & 1u) ? -u[j] : u[j];
+  uint64_t P[16];
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
+  for (int k = 0; k < 16; ++k) P[k] = f32x2_pack(__fadd_rn(u[2 * k], u[2 * k + 1]), __fsub_rn(u[2 * k], u[2 * k + 1]));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((i & h) == 0) {
-        const float a = u[i], b = u[i + h];
-        u[i] = __fadd_rn(a, b);
-        u[i + h] = __fsub_rn(a, b);
+  for (int hh = 1; hh < 16; hh <<= 1) {            // h = 2 hh
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if ((k & hh) == 0) {
+        const uint64_t a = P[k], b = P[k + hh];
+        P[k] = f32x2_add(a, b);
+        P[k + hh] = f32x2_sub(a, b);
       }
     }
   }
+  const uint64_t cc = f32x2_pack(kHadC, kHadC);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) u[j] = __fmul_rn(u[j], kHadC);
+  for (int k = 0; k < 16; ++k) f32x2_unpack(f32x2_mul(P[k], cc), u[2 * k], u[2 * k + 1]);
 }
 
-__device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+// Bits of the largest |v| of 32 float32 values: a tree of three-input
+// NaN-propagating maxima over the magnitudes, so a NaN anywhere gives NaN
+// bits and an infinity 0x7F800000 -- the same classification and, for
+// finite blocks, the same bits as the unsigned maximum of the sign-cleared
+// words.
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t amax32_float(const float (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = fmax3_nan(fabsf(v[3 * i]), fabsf(v[3 * i + 1]), fabsf(v[3 * i + 2]));
+  t[10] = fmax3_nan(fabsf(v[30]), fabsf(v[31]), 0.0f);
+  const float m = fmax3_nan(fmax3_nan(t[0], t[1], t[2]), fmax3_nan(t[3], t[4], t[5]), fmax3_nan(t[6], t[7], t[8]));
+  return __float_as_uint(fmax3_nan(m, t[9], t[10])) & 0x7FFFFFFFu;
+}
 
 // Packed bf16x2 running max of magnitudes, NaN-propagating, one instruction
 // per word: each half becomes max(|m|, |w|) with the XOR of the two signs;
@@ -246,7 +296,12 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
                                                   uint64_t idx0, uint64_t istep, uint32_t (&out)[8]) {
   const bool bad = ab >= 0x7F800000u;                 // NaN or Inf in the block
   const int e = scale_exp<FMT>(bad ? 0u : ab, p.ceil_mode);
-  const float m = exp2_neg(e);
+  float vm[32];                                       // v * 2^-e, packed products
+  {
+    const uint64_t mm = f32x2_splat(exp2_neg(e));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) f32x2_unpack(f32x2_mul(f32x2_pack(v[2 * k], v[2 * k + 1]), mm), vm[2 * k], vm[2 * k + 1]);
+  }
   float y[32];
   if (EXTRA && p.rounding == MXQ_SR4 && istep == 1) {
     // a row block: 32 consecutive indices from a multiple of 32, so the
@@ -256,22 +311,22 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
       const uint64_t c = (idx0 >> 2) + k;
       const u32x4 w =
           philox4x32_10(u32x4{static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u}, p.sr_k0, p.sr_k1);
-      y[4 * k] = sr_round<FMT>(__fmul_rn(v[4 * k], m), w.x);
-      y[4 * k + 1] = sr_round<FMT>(__fmul_rn(v[4 * k + 1], m), w.y);
-      y[4 * k + 2] = sr_round<FMT>(__fmul_rn(v[4 * k + 2], m), w.z);
-      y[4 * k + 3] = sr_round<FMT>(__fmul_rn(v[4 * k + 3], m), w.w);
+      y[4 * k] = sr_round<FMT>(vm[4 * k], w.x);
+      y[4 * k + 1] = sr_round<FMT>(vm[4 * k + 1], w.y);
+      y[4 * k + 2] = sr_round<FMT>(vm[4 * k + 2], w.z);
+      y[4 * k + 3] = sr_round<FMT>(vm[4 * k + 3], w.w);
     }
   } else if (EXTRA && p.rounding == MXQ_SR4) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      y[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw4(idx0 + j * istep, p.sr_k0, p.sr_k1));
+      y[j] = sr_round<FMT>(vm[j], sr_draw4(idx0 + j * istep, p.sr_k0, p.sr_k1));
   } else if (EXTRA && p.rounding == MXQ_SR) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      y[j] = sr_round<FMT>(__fmul_rn(v[j], m), sr_draw(idx0 + j * istep, p.sr_k0, p.sr_k1));
+      y[j] = sr_round<FMT>(vm[j], sr_draw(idx0 + j * istep, p.sr_k0, p.sr_k1));
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(v[j], m);
+    for (int j = 0; j < 32; ++j) y[j] = vm[j];
   }
   if constexpr (FMT == MXQ_E2M1) {
 #pragma unroll
@@ -504,9 +559,7 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
             uint32_t ab;
             if (p.hadamard) {
               hadamard32(v, signs);
-              ab = 0;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) ab = max(ab, absbits(v[q]));
+              ab = amax32_float(v);
             } else {
               ab = amax_bf16x32(w);
             }
@@ -584,9 +637,7 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
             uint32_t ab = abw;
             if (p.hadamard) {
               hadamard32(v, signs);
-              ab = 0;
-#pragma unroll
-              for (int k = 0; k < 32; ++k) ab = max(ab, absbits(v[k]));
+              ab = amax32_float(v);
             }
             const uint64_t idx0 = static_cast<uint64_t>(r0 + rb * 32) * static_cast<uint64_t>(p.cols) + (c0 + cl);
             scb[half] = quant_block32<FMT, EXTRA>(v, ab, p, idx0, static_cast<uint64_t>(p.cols), out);
