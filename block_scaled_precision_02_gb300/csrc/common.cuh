@@ -266,6 +266,33 @@ __device__ __forceinline__ uint64_t f32x2_splat(float m) {
   return r;
 }
 
+// Packed pairs of float32 (first element in the low half) and the packed
+// operations on them: each half rounds to nearest exactly as the scalar
+// operation would.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // FP8 codes of lo(wa), hi(wa), lo(wb), hi(wb) -- four bf16 values (packed
 // two per word, element 2i in the low half) each multiplied by m (RN, with
 // one packed f32x2 multiply per pair) and converted RNE-saturating.  Code of
@@ -356,6 +383,28 @@ __device__ __forceinline__ int scale_exp(uint32_t ab, int ceil_mode) {
   int e = static_cast<int>(ab >> 23) - 127 - FmtInfo<FMT>::Ed;
   if (ceil_mode && (ab & 0x7FFFFFu) > FmtInfo<FMT>::md) e += 1;
   return max(-127, min(127, e));
+}
+
+// NaN-propagating maximum of three float32 values: a NaN operand gives NaN,
+// subnormals are kept.
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Bits of the largest magnitude among 32 float32 values, mag(j) = |v_j|, by
+// a tree of 16 three-input maxima: a NaN anywhere gives NaN bits, an
+// infinity 0x7F800000, otherwise the largest |v_j| exactly -- the same
+// classification and bits as the unsigned maximum of the sign-cleared words.
+template <typename Mag>
+__device__ __forceinline__ uint32_t amax32_tree(Mag mag) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = fmax3_nan(mag(3 * i), mag(3 * i + 1), mag(3 * i + 2));
+  t[10] = fmax3_nan(mag(30), mag(31), 0.0f);
+  const float u = fmax3_nan(fmax3_nan(t[0], t[1], t[2]), fmax3_nan(t[3], t[4], t[5]), fmax3_nan(t[6], t[7], t[8]));
+  return __float_as_uint(fmax3_nan(u, t[9], t[10])) & 0x7FFFFFFFu;
 }
 
 // 2^-e as float32 (e in [-127, 125] here, so the result is a normal number).

@@ -355,31 +355,10 @@ __device__ __forceinline__ uint32_t mma_idesc(const Params& p, int n, int m, int
   else return instr_desc(p.a_type, p.b_type, n, m, KIND == KIND_MXF4 ? (kk & 1) * 2 : kk);
 }
 
-// NaN-propagating maxima of two or three float32 values (a NaN operand
-// gives NaN; no flush of subnormals).
-__device__ __forceinline__ float fmax2n(float a, float b) {
-  float d;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-__device__ __forceinline__ float fmax3n(float a, float b, float c) {
-  float d;
-  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Bits of the largest magnitude among 32 float32 words, by a tree of
-// three-input maxima over the absolute values: a NaN anywhere gives NaN
-// bits, an infinity 0x7F800000, otherwise the largest |v| exactly -- the same
-// as the unsigned maximum of the sign-cleared bits.
+// Bits of the largest magnitude among the 32 float32 words of a block
+// (NaN anywhere: NaN bits; an infinity: 0x7F800000).
 __device__ __forceinline__ uint32_t amax32_bits(const uint32_t (&v)[32]) {
-  auto a = [&](int j) { return fabsf(__uint_as_float(v[j])); };
-  float t[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i) t[i] = fmax3n(a(3 * i), a(3 * i + 1), a(3 * i + 2));
-  t[10] = fmax2n(a(30), a(31));
-  const float u = fmax3n(fmax3n(t[0], t[1], t[2]), fmax3n(t[3], t[4], t[5]), fmax3n(t[6], t[7], t[8]));
-  return __float_as_uint(fmax3n(u, t[9], t[10])) & 0x7FFFFFFFu;
+  return amax32_tree([&](int j) { return fabsf(__uint_as_float(v[j])); });
 }
 
 // FP8 codes of four float32 words each multiplied by m (mm = m twice; one

@@ -133,33 +133,6 @@ __device__ __forceinline__ uint32_t sr_draw4(uint64_t idx, uint32_t k0, uint32_t
 
 constexpr float kHadC = 0.17677669529663688f;  // float32 nearest 1/sqrt(32)
 
-// Packed pairs of float32 (first element in the low half) and the packed
-// operations on them: each half rounds to nearest exactly as the scalar
-// operation would.
-__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
-}
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
 // Fixed-sign 32-point Hadamard of one block held by one thread:
 // u_j = s_j v_j; butterflies h = 1, 2, 4, 8, 16 in that order,
 // (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h}) for (i & h) == 0;
@@ -188,23 +161,10 @@ __device__ __forceinline__ void hadamard32(float (&u)[32], uint32_t signs) {
   for (int k = 0; k < 16; ++k) f32x2_unpack(f32x2_mul(P[k], cc), u[2 * k], u[2 * k + 1]);
 }
 
-// Bits of the largest |v| of 32 float32 values: a tree of three-input
-// NaN-propagating maxima over the magnitudes, so a NaN anywhere gives NaN
-// bits and an infinity 0x7F800000 -- the same classification and, for
-// finite blocks, the same bits as the unsigned maximum of the sign-cleared
-// words.
-__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
-  float d;
-  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
+// Bits of the largest |v| of a block of 32 float32 values (NaN anywhere:
+// NaN bits; an infinity: 0x7F800000).
 __device__ __forceinline__ uint32_t amax32_float(const float (&v)[32]) {
-  float t[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i) t[i] = fmax3_nan(fabsf(v[3 * i]), fabsf(v[3 * i + 1]), fabsf(v[3 * i + 2]));
-  t[10] = fmax3_nan(fabsf(v[30]), fabsf(v[31]), 0.0f);
-  const float m = fmax3_nan(fmax3_nan(t[0], t[1], t[2]), fmax3_nan(t[3], t[4], t[5]), fmax3_nan(t[6], t[7], t[8]));
-  return __float_as_uint(fmax3_nan(m, t[9], t[10])) & 0x7FFFFFFFu;
+  return amax32_tree([&](int j) { return fabsf(v[j]); });
 }
 
 // Packed bf16x2 running max of magnitudes, NaN-propagating, one instruction
