@@ -366,10 +366,10 @@ __device__ __forceinline__ int job_of(const QuantLaunch<NJ>& L, int tile) {
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT, int NJ>
-__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8,
+__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, 8,
                                                ORIENT == MXQ_ROW ? 1024 : 2048>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams p0) {
-  using T = TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
+  using T = TileCfg<NSTG, NOUT, EXTRA, 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
   constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
@@ -457,13 +457,20 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
 
   // This warp's part of every tile.
   const bool row_warp = warp < ROW_WARPS;
-  const int col_band = DO_COL ? (DUAL ? warp - 4 : (DO_ROW ? -1 : warp)) : -1;
+  // column only: warps 0-3 take the even tiles of the CTA, warps 4-7 the odd.
+  // With an even number of stages each stage then serves one group only, so
+  // a group's waits on a stage follow that stage's phases in order (with an
+  // odd count a group could pass a wait on the other group's phase).
+  constexpr bool SPLIT = DO_COL && !DO_ROW;
+  constexpr int ISTEP = SPLIT ? 2 : 1;
+  static_assert(!SPLIT || NSTG % 2 == 0, "column-only launches need an even stage count");
+  const int col_band = DO_COL ? (DUAL ? warp - 4 : (DO_ROW ? -1 : (warp & 3))) : -1;
   const bool col_warp = DO_COL && col_band >= 0 && col_band < 4;
   const int ro = row_warp ? warp * RR : 0;           // first tile row of a row warp
 
   uint32_t amax_acc = 0;   // per-tensor: running max of |x| bits
   if (row_warp || col_warp) {
-    for (int i = 0;; ++i) {
+    for (int i = SPLIT ? (warp >> 2) : 0;; i += ISTEP) {
       const int tile = blockIdx.x + i * gridDim.x;
       if (tile >= ntiles || *abort_flag) break;
       const int jb = job_of(L, tile);
@@ -476,7 +483,7 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
         break;
       }
       const uint8_t* in = in_s + s * T::IN_BYTES;
-      uint8_t* stg = stg_s + (warp * NOUT + i % NOUT) * T::STG;
+      uint8_t* stg = stg_s + (warp * NOUT + (i / ISTEP) % NOUT) * T::STG;
       // this buffer was last read by the bulk store of tile i - NOUT
       if (lane == 0) {
         if constexpr (NOUT == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -790,8 +797,10 @@ constexpr int QSTG = MXQ_QUANT_STG;
 
 template <int FMT, int ORIENT, bool PT, bool EXTRA, int NJ>
 int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
-  constexpr int NST = EXTRA ? QNST_EXTRA : QNST;
-  using T = TileCfg<NST, QSTG, EXTRA, ORIENT == MXQ_COL ? 4 : 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
+  // column-only launches split the tiles between two warp groups, which
+  // needs an even stage count (two per group for the lean variants)
+  constexpr int NST = EXTRA ? QNST_EXTRA : (ORIENT == MXQ_COL ? 4 : QNST);
+  using T = TileCfg<NST, QSTG, EXTRA, 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
   auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, NST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
