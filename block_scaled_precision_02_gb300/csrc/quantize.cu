@@ -26,7 +26,9 @@
 //  * Dual orientation: warps 0-3 take 32 rows each (one lane per row, both
 //    1 x 32 blocks of the row); warps 4-7 take a 32-row band each (one lane
 //    per two adjacent columns, two 32 x 1 blocks in registers).  Row only:
-//    eight warps of 16 rows (one block per lane).  Column only: warps 0-3.
+//    eight warps of 16 rows (one block per lane).  Column only: warps 0-3
+//    take the bands of the CTA's even tiles, warps 4-7 those of its odd
+//    tiles (an even number of stages keeps each stage with one group).
 //  * The column copy is staged transposed, so it leaves as rows of q_col.
 //    Scales leave from the lanes that computed them, in the requested layout
 //    (canonical, or the GEMM's 512-byte tensor-core chunks).
@@ -53,7 +55,7 @@ namespace mxq {
 constexpr int TR = 128;                     // tile rows
 constexpr int BOX_BYTES = TR * 64 * 2;      // one TMA load box: 128 rows x 64 bf16 (16 KiB)
 
-template <int NSTG, int NOUT, bool EXTRA, int SW = 8, int STG_ = 2048>
+template <int NSTG, int NOUT, bool EXTRA, int STG_ = 2048>
 struct TileCfg {
   static constexpr int TC = 64;                     // tile columns
   static constexpr int THREADS = 256;
@@ -62,11 +64,10 @@ struct TileCfg {
   // one staging buffer of one warp: a dual launch's 32 rows (or 64 columns)
   // of codes, 2 KiB; a row-only warp's 16 rows, 1 KiB
   static constexpr int STG = STG_;
-  // SW warps write codes: all eight, or the four column warps of a
-  // column-only launch (warps 0-3).  Column-only and row-only launches
-  // thereby need 65 KB of shared memory, which fits a third CTA per SM.
-  static constexpr int SWARPS = SW;
-  static constexpr int SMEM = NSTG * IN_BYTES + SW * NOUT * STG + 256 + 1024;
+  // every warp writes codes through its own staging buffers; a row-only
+  // launch (1 KiB buffers) thereby needs 65 KB of shared memory, which fits
+  // a third CTA per SM
+  static constexpr int SMEM = NSTG * IN_BYTES + NW * NOUT * STG + 256 + 1024;
   // resident CTAs per SM the registers are budgeted for
   static constexpr int MIN_BLOCKS = EXTRA ? 2 : (SMEM <= 70 * 1024 ? 3 : 2);
 };
@@ -366,10 +367,10 @@ __device__ __forceinline__ int job_of(const QuantLaunch<NJ>& L, int tile) {
 // EXTRA: compile the stochastic-rounding and Hadamard paths (selected at run
 // time by the parameters); without it the kernel is the lean RNE variant.
 template <int FMT, int ORIENT, bool PERTENSOR, bool EXTRA, int NSTG, int NOUT, int NJ>
-__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA, 8,
+__global__ void __launch_bounds__(256, TileCfg<NSTG, NOUT, EXTRA,
                                                ORIENT == MXQ_ROW ? 1024 : 2048>::MIN_BLOCKS)
 quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams p0) {
-  using T = TileCfg<NSTG, NOUT, EXTRA, 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
+  using T = TileCfg<NSTG, NOUT, EXTRA, ORIENT == MXQ_ROW ? 1024 : 2048>;
   constexpr int TC = T::TC;
   constexpr bool DO_ROW = (ORIENT & MXQ_ROW) != 0;
   constexpr bool DO_COL = (ORIENT & MXQ_COL) != 0;
@@ -386,8 +387,8 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* in_s = smem;                                   // NSTG x 16 KiB stages
-  uint8_t* stg_s = in_s + NSTG * T::IN_BYTES;             // per code-writing warp NOUT staging buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + T::SWARPS * NOUT * T::STG);   // full[NSTG]
+  uint8_t* stg_s = in_s + NSTG * T::IN_BYTES;             // per warp NOUT staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + T::NW * NOUT * T::STG);   // full[NSTG]
   uint32_t* cnt = reinterpret_cast<uint32_t*>(bars + NSTG);       // readers done with each stage
   int* last_use = reinterpret_cast<int*>(cnt + NSTG);             // latest load issued into each stage
   uint32_t* red = reinterpret_cast<uint32_t*>(last_use + NSTG);   // per-warp amax (per-tensor)
@@ -800,7 +801,7 @@ int launch_tiles(const QuantLaunch<NJ>& L, cudaStream_t st) {
   // column-only launches split the tiles between two warp groups, which
   // needs an even stage count (two per group for the lean variants)
   constexpr int NST = EXTRA ? QNST_EXTRA : (ORIENT == MXQ_COL ? 4 : QNST);
-  using T = TileCfg<NST, QSTG, EXTRA, 8, ORIENT == MXQ_ROW ? 1024 : 2048>;
+  using T = TileCfg<NST, QSTG, EXTRA, ORIENT == MXQ_ROW ? 1024 : 2048>;
   auto kern = quant_tiles_kernel<FMT, ORIENT, PT, EXTRA, NST, QSTG, NJ>;
   // stages, per-warp staging buffers, barriers and counters (256 B), alignment slack
   constexpr int smem = T::SMEM;
