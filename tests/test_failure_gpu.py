@@ -34,6 +34,28 @@ def test_quantizer_wait_expires_and_context_survives(lib):
     assert lib.last_device_status() == 0
 
 
+def test_column_only_wait_expires_and_context_survives(lib):
+    """A column-only launch splits each CTA's tiles between two warp groups
+    (even and odd tiles, each on its own stages).  With one group's first
+    stage never landing, that group times out, the other group's tiles and
+    the loads still in flight end normally, the status reads TIMEOUT, and
+    the next call is exact.  4096 x 4096 gives every CTA many tiles."""
+    L = lib.load()
+    dev = torch.device("cuda")
+    x = inputs.activations(4096, 4096, seed=3)
+    xd = x.to(dev)
+    assert lib.last_device_status() == 0
+    assert L.mxq_test_stall_next_launch(1) == 0
+    lib.mx_quantize(xd, "e4m3", "col", "floor")
+    assert lib.last_device_status() == MXQ_ERR_TIMEOUT
+    out = lib.mx_quantize(xd, "e4m3", "col", "floor")
+    for r0 in (0, 2048, 3840):                       # 256-row slabs: their column blocks
+        ref = omx.quantize(f64(x)[r0:r0 + 256], F.E4M3, omx.COL, omx.FLOOR)
+        assert_bytes_equal(np_(out[2])[:, r0:r0 + 256], ref["q_col"], f"q_col after recovery, rows {r0}+")
+        assert_bytes_equal(np_(out[3])[:, r0 // 32:r0 // 32 + 8], ref["s_col"], f"s_col after recovery, rows {r0}+")
+    assert lib.last_device_status() == 0
+
+
 def test_gemm_wait_expires_and_context_survives(lib):
     L = lib.load()
     dev = torch.device("cuda")
