@@ -485,7 +485,7 @@ quant_tiles_kernel(const __grid_constant__ QuantLaunch<NJ> L, const QuantParams 
       }
       const uint8_t* in = in_s + s * T::IN_BYTES;
       uint8_t* stg = stg_s + (warp * NOUT + (i / ISTEP) % NOUT) * T::STG;
-      // this buffer was last read by the bulk store of tile i - NOUT
+      // this buffer was last read by the bulk store of this warp's tile NOUT tiles back
       if (lane == 0) {
         if constexpr (NOUT == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         else bulk_wait_read_all();
